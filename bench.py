@@ -1,0 +1,346 @@
+#!/usr/bin/env python
+"""Fused GQA attention forward benchmark on GB300.
+
+One step = one launch of the fused attention forward over the long causal GQA
+prefill workload (B=1, Hq=32, Hkv=8, N=32768, D=128, bf16) with inputs
+resident in HBM.  Prints one JSON line (rank 0):
+  value      TFLOP/s over all ranks, FLOPs counted 2*B*Hq*N^2*D (causal);
+  roofline   the kernel's achieved TFLOP/s against the measured bf16 peak;
+  e2e        the same metric with host->device input copies and the
+             device->host read of O and LSE inside the timed region;
+  cpu_baseline  the float64 oracle timed on the host cores on a row sample.
+``--impl reference`` times the float64 oracle alone (CPU) on the same metric.
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gqa_attention_forward_gb300 import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (causal FLOPs) on 1 GB300; % of dense FP16/BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "long_prefill_causal_gqa_bf16_n32768"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ CPU oracle
+def row_flops(w, rows: np.ndarray) -> float:
+    """Counted FLOPs of the selected output rows: 4*D per allowed key."""
+    i = rows % w.N
+    keys = (i + 1) if w.causal else np.full_like(i, w.N)
+    return float(4.0 * w.D * keys.sum())
+
+
+class OracleSampler:
+    """Times the float64 oracle on random output rows of a workload."""
+
+    def __init__(self, w, seed: int = 4242):
+        import oracle
+
+        self.oracle = oracle
+        self.w = w
+        x = workloads.make_inputs(w)
+        self.q = x["q"].reshape(-1, w.D)
+        self.k = oracle.widen(x["k"], w.dtype)
+        self.v = oracle.widen(x["v"], w.dtype)
+        self.rng = np.random.default_rng(seed)
+        self.threads = 0
+
+    def run(self, n_rows: int):
+        w = self.w
+        rows = np.sort(self.rng.integers(0, w.B * w.Hq * w.N, size=n_rows))
+        q_rows = self.oracle.widen(self.q[rows], w.dtype)
+        t0 = time.perf_counter()
+        _, _, self.threads = self.oracle.attention_rows(q_rows, rows, self.k, self.v, w.Hq, w.scale,
+                                                        w.causal)
+        return row_flops(w, rows), time.perf_counter() - t0
+
+
+def cpu_baseline(w, seconds: float):
+    s = OracleSampler(w)
+    flops, secs, rows = 0.0, 0.0, 0
+    n = 64
+    while secs < seconds:
+        f, t = s.run(n)
+        flops, secs, rows = flops + f, secs + t, rows + n
+        if t < seconds / 8:
+            n *= 2
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": s.threads, "kind": "oracle",
+            "sample": f"{rows} random output rows of {w.name} (float64 C oracle, "
+                      f"{secs:.1f} s, {flops / 1e9:.1f} GFLOP counted 4*D per allowed key)"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def to_dev(bits, dtype, device):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16 if dtype == "f16" else torch.bfloat16).to(device)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from gqa_attention_forward_gb300 import binding
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w, seed=w.seed + rank)  # each rank: its own replica
+    q, k, v = (to_dev(x[n], w.dtype, device) for n in "qkv")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    dcode = binding.ATTN_BF16 if w.dtype == "bf16" else binding.ATTN_F16
+    args_c = (w.B, w.Hq, w.Hkv, w.N, w.D, w.scale, w.causal, dcode)
+
+    def step():
+        st = binding.attn_fwd(q, k, v, o, lse, *args_c, stream)
+        if st != binding.ATTN_OK:
+            raise binding.AttnError(st, "attn_fwd")
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = binding.attn_last_device_error(stream)
+    if st != binding.ATTN_OK:
+        raise binding.AttnError(st, "warm-up")
+
+    # ---- device-resident timing: K launches, one event pair per launch
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(device.index if world == 1 else local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(K):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    st = binding.attn_last_device_error(stream)
+    if st != binding.ATTN_OK:
+        raise binding.AttnError(st, "timed region")
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * w.flops * K / (total_ms / 1e3) / 1e12
+    kern_ms = float(np.mean(per_launch_ms))
+    achieved = w.flops / (kern_ms / 1e3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> attn_fwd -> O, LSE back to host
+    hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(x[n]).view(np.int16)).pin_memory()
+                  for n in "qkv")
+    ho = torch.empty(o.numel(), dtype=torch.int16).pin_memory()
+    hl = torch.empty(lse.numel(), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (t.view(torch.int16).view(-1) for t in (q, k, v))
+    do = o.view(torch.int16).view(-1)
+    E = max(1, min(args.e2e_steps, K))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        dq.copy_(hq.view(-1), non_blocking=True)
+        dk.copy_(hk.view(-1), non_blocking=True)
+        dv.copy_(hv.view(-1), non_blocking=True)
+        step()
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(lse.view(-1), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * 2 + hl.numel() * 4
+
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        long_region = total_ms > 1000.0
+        peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms / K, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded i.i.d. normal, see workloads.py)",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "D": w.D,
+                       "causal": w.causal,
+                       "flops_per_step": w.flops,
+                       "flop_convention": "2*B*Hq*N^2*D causal, 4*B*Hq*N^2*D non-causal",
+                       "l2": "inputs larger than L2 (no flush)" if
+                             (2 * w.B * (w.Hq + 2 * w.Hkv) * w.N * w.D) > 129e6 else
+                             "inputs smaller than L2 (not flushed)",
+                       "parallelism": f"replica x{world}"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_src} "
+                                        f"{'sustained' if long_region else 'burst'} bf16",
+                         "kernel": "gqa::attn_fwd_kernel", "kernel_ms": round(kern_ms, 4),
+                         "frac_of_2250_nominal": round(achieved / 2250.0, 4)},
+            "e2e": {"value": round(world * w.flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": K,
+            "clocks": clock_info,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    s = OracleSampler(w)
+    rows_per_step = 256 if w.causal else 64
+    for _ in range(max(args.warmup, 1)):
+        s.run(16)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, t = s.run(rows_per_step)
+        flops += f
+        secs += t
+    value = flops / secs / 1e12
+    sample = (f"{args.steps} steps x {rows_per_step} random output rows of {w.name} "
+              f"(float64 C oracle on the host cores)")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded i.i.d. normal)", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
+                       "D": w.D, "causal": w.causal},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": s.threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

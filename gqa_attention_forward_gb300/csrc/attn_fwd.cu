@@ -1,0 +1,553 @@
+// Fused grouped-query attention forward for GB300 (sm_103a).
+//
+// O = softmax(mask(Q K^T * scale)) V with the online-softmax update of the
+// page "从零开始写Qwen3" (deepseek.csdn.net/6a3201f8..., sections "在线softmax"
+// and "FlashAttention"): each CTA owns one 128-row query tile, streams the
+// key/value tiles it needs, keeps a running row max m and row sum l in fp32,
+// rescales the output accumulator when m grows and normalises once at the
+// end.  The score matrix never leaves the SM.
+//
+// Hardware mapping:
+//   * warp 0 (one lane): TMA producer.  Q once; then K_j, V_j alternately into
+//     a kStages-deep ring of 128-byte-swizzled shared-memory tiles guarded by
+//     full / empty mbarriers.
+//   * warp 1 (one lane): tcgen05 MMA issuer.  S = Q K_j^T into TMEM columns
+//     [0, 128); O += P V_j into TMEM columns [128, 128 + D).  Completion is
+//     signalled with tcgen05.commit onto mbarriers.
+//   * warps 4-7: softmax.  Thread t owns query row t (TMEM lane t): it reads
+//     its 128 scores with tcgen05.ld, applies the causal / tail mask, updates
+//     m and l, writes P (rounded to the input type) into shared memory in the
+//     UMMA K-major swizzled layout, and rescales its O row in TMEM when m
+//     grows.  Finally it normalises O, stores it and the log-sum-exp.
+//
+// Causal tiles above the diagonal are never visited and only the diagonal
+// tile is masked (page "从零开始写Qwen3", deepseek.csdn.net/6a31faef..., sections
+// "改进2-KV只读取下三角" and "改进3-两阶段计算").  The exponent uses exp2 with
+// scale*log2(e) folded into one FMA (same page, "优化点6-使用exp2而不是exp").
+// Query tiles of one (batch, head) are adjacent in launch order so their K/V
+// reads hit L2 (same page, "改进1-使用正确的grid").
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "attn_fwd_ws.cuh"
+#include "gqa_attn.h"
+#include "kernel_common.cuh"
+#include "sm103_ptx.cuh"
+
+namespace gqa {
+
+constexpr int kStages = 4;     // K/V tiles in flight
+constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 4..7 softmax
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemO = 128;  // first TMEM column of the O accumulator
+
+template <int D>
+struct Layout {
+    static constexpr int kAtoms = D / 64;           // 64 halfs = one 128-byte swizzle row
+    static constexpr int kAtomBytes = 128 * 128;    // 128 rows x 128 B
+    static constexpr int kTileBytes = kAtoms * kAtomBytes;
+    static constexpr int kQ = 0;
+    static constexpr int kKV = kQ + kTileBytes;
+    static constexpr int kP = kKV + kStages * kTileBytes;
+    static constexpr int kPBytes = 2 * kAtomBytes;  // P tile: 128 x 128 halfs
+    static constexpr int kBar = kP + kPBytes;
+    static constexpr int kNumBars = 1 + 2 * kStages + 4;
+    static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 4;
+    static constexpr int kUsed = kAbort + 4;
+    static constexpr int kAlloc = kUsed + 1024;  // slack to align the base to 1024 B
+};
+
+template <int D, bool kBF16, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t sQ = base + L::kQ, sKV = base + L::kKV, sP = base + L::kP;
+    const uint32_t bar0 = base + L::kBar;
+    const uint32_t q_full = bar0;
+    auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
+    const uint32_t s_full = bar0 + 8u * (1 + 2 * kStages);
+    const uint32_t p_full = bar0 + 8u * (2 + 2 * kStages);
+    const uint32_t o_full = bar0 + 8u * (3 + 2 * kStages);
+    const uint32_t mma_done = bar0 + 8u * (4 + 2 * kStages);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Query tiles of one (b, hq) are adjacent; within it the longest causal
+    // rows come first.
+    const int q_tile = p.n_qtiles - 1 - static_cast<int>(blockIdx.x % p.n_qtiles);
+    const int bh = static_cast<int>(blockIdx.x / p.n_qtiles);  // b*Hq + hq
+    const int kvh = bh / p.group;                               // b*Hkv + hq/(Hq/Hkv)
+    const int q0 = q_tile * kBM;
+    const int n_kv = kCausal ? (q_tile + 1) : p.n_kv_tiles;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, kBM);
+        mbar_init(o_full, 1);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (*abort_flag) return;  // another CTA of this launch already gave up
+    if (warp == 1) {
+        tmem_alloc(base + L::kTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            bool issued_q = false;
+            if (!p.inject_stall) {
+                mbar_arrive_expect_tx(q_full, L::kTileBytes);
+#pragma unroll
+                for (int a = 0; a < L::kAtoms; ++a)
+                    tma_load_3d(sQ + a * L::kAtomBytes, &tmQ, a * 64, q0, bh, q_full);
+                issued_q = true;
+            }
+            int stage = 0;
+            uint32_t phase = 0, used = 0, last_phase = 0;
+            bool ok = true;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                for (int t = 0; t < 2; ++t) {
+                    if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(kv_full(stage), L::kTileBytes);
+                    const void *tm = t ? static_cast<const void *>(&tmV) : static_cast<const void *>(&tmK);
+#pragma unroll
+                    for (int a = 0; a < L::kAtoms; ++a)
+                        tma_load_3d(sKV + stage * L::kTileBytes + a * L::kAtomBytes, tm, a * 64,
+                                    j * kBN, kvh, kv_full(stage));
+                    used |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy issued must have landed before the CTA may exit.
+            if (issued_q) drain_bar(q_full, 0, p);
+            for (int s = 0; s < kStages; ++s)
+                if (used >> s & 1u) drain_bar(kv_full(s), last_phase >> s & 1u, p);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, kBM, kBN, false);
+            constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, kBM, D, true);
+            const uint32_t tS = tmem, tO = tmem + kTmemO;
+            bool ok = wait_bar(q_full, 0, p, abort_flag);
+            tc_fence_after();
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                // S = Q K_j^T   (A = Q, B = K: both K-major, 128-byte swizzle)
+                if (!wait_bar(kv_full(stage), phase, p, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t sK = sKV + stage * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+                    mma_f16_ss(tS, sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(sK + koff, 16, 1024),
+                               idesc_qk, kk > 0);
+                }
+                mma_commit(s_full);
+                mma_commit(kv_empty(stage));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                // O += P V_j   (A = P: K-major; B = V: MN-major, 64-wide chunks
+                // of D at LBO = one atom, 8-row groups of keys at SBO = 1024 B)
+                if (!wait_bar(p_full, j & 1, p, abort_flag)) break;
+                tc_fence_after();
+                if (!wait_bar(kv_full(stage), phase, p, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t sV = sKV + stage * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint32_t poff = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+                    mma_f16_ss(tO, sdesc_sw128(sP + poff, 16, 1024),
+                               sdesc_sw128(sV + kk * 2048, L::kAtomBytes, 1024), idesc_pv,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(o_full);
+                mma_commit(kv_empty(stage));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // TMEM and shared memory stay alive until every issued MMA is done.
+            mma_commit(mma_done);
+            drain_bar(mma_done, 0, p);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------- softmax rows
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // row within the tile == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tO = tmem + kTmemO + lane_off;
+        const float c = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        const uint32_t prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!__all_sync(0xffffffffu, wait_bar(s_full, j & 1, p, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            __syncwarp();
+            uint32_t s[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                tmem_ld32(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q]));
+            tmem_ld_wait(s);
+            const int kv0 = j * kBN;
+            if (kCausal) {
+                if (kv0 == q0) {  // diagonal tile: keep key c <= row r
+#pragma unroll
+                    for (int cc = 0; cc < 128; ++cc)
+                        if (cc > r) s[cc] = __float_as_uint(-INFINITY);
+                }
+            } else if (kv0 + kBN > p.N) {  // ragged last tile: keys >= N are absent
+                const int lim = p.N - kv0;
+#pragma unroll
+                for (int cc = 0; cc < 128; ++cc)
+                    if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
+            }
+            float mt = u2f(s[0]);
+#pragma unroll
+            for (int cc = 1; cc < 128; ++cc) mt = fmaxf(mt, u2f(s[cc]));
+            const float m_new = fmaxf(m, mt);
+            const float alpha = ex2_approx((m - m_new) * c);  // 0 on the first tile
+            if (j > 0) {
+                // P V_{j-1} must be done: it reads the P buffer and writes O.
+                if (!__all_sync(0xffffffffu, wait_bar(o_full, (j - 1) & 1, p, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, m_new > m)) {
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * q, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(u2f(o[i]) * alpha);
+                        tmem_st32(tO + 32 * q, o);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            m = m_new;
+            l *= alpha;
+            const float mc = m * c;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                float e[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    e[t] = ex2_approx(fmaf(u2f(s[ch * 8 + t]), c, -mc));
+                    l += e[t];
+                }
+                const uint32_t addr = prow + (ch >> 3) * L::kAtomBytes + (((ch & 7) ^ (r & 7)) << 4);
+                st_shared_v4(addr, pack2<kBF16>(e[0], e[1]), pack2<kBF16>(e[2], e[3]),
+                             pack2<kBF16>(e[4], e[5]), pack2<kBF16>(e[6], e[7]));
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        // ---------------------------------------------------- epilogue
+        if (ok && __all_sync(0xffffffffu, wait_bar(o_full, (n_kv - 1) & 1, p, abort_flag))) {
+            tc_fence_after();
+            __syncwarp();
+            const int row = q0 + r;
+            const float inv_l = 1.f / l;
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.N + row) * (D * 2);
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * q, o);
+                tmem_ld_wait(o);
+                if (row < p.N) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack2<kBF16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        st_global_v4(orow + q * 64 + v * 16, w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                                     w[4 * v + 3]);
+                }
+            }
+            if (p.lse != nullptr && row < p.N)
+                p.lse[static_cast<size_t>(bh) * p.N + row] = (m * c + log2f(l)) * 0.6931471805599453f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace gqa
+
+// =================================================================== host
+namespace {
+
+thread_local char t_last_cuda_error[256] = "";
+std::atomic<unsigned int> g_launch_seq{1};
+std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
+std::atomic<int> g_inject_stall{0};
+
+void note_cuda_error(cudaError_t e, const char *where) {
+    std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", where, cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [rows = BH * N, D] viewed as 3-D (D, N, BH) so that a box never crosses
+// from one head into the next: rows past N read as zeros.
+bool encode_qkv_map(CUtensorMap *map, const void *base, bool bf16, int D, int N, long long BH) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_dev_state[kMaxDevices];      // 0 unknown, 1 sm_103, -1 other
+int g_dev_sms[kMaxDevices];        // multiprocessor count
+unsigned g_dev_smem_set[kMaxDevices];  // bit per kernel instantiation
+std::atomic<int> g_kernel_choice{0};   // 0 persistent warp-specialised, 1 one CTA per query tile
+
+attn_status_t check_device(int *dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaGetDevice");
+        return ATTN_ERR_NODEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NODEVICE;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev_state[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            note_cuda_error(cudaGetLastError(), "cudaDeviceGetAttribute");
+            return ATTN_ERR_NODEVICE;
+        }
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_dev_sms[dev] = sms > 0 ? sms : 1;
+        g_dev_state[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    *dev_out = dev;
+    return g_dev_state[dev] == 1 ? ATTN_OK : ATTN_ERR_NODEVICE;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+attn_status_t launch(int dev, int kid, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                     gqa::Params prm, cudaStream_t stream) {
+    const bool persistent = g_kernel_choice.load() == 0;
+    auto kern = persistent ? gqa::attn_fwd_ws_kernel<D, BF16, CAUSAL> : gqa::attn_fwd_kernel<D, BF16, CAUSAL>;
+    const int smem = persistent ? gqa::WsLayout<D>::kAlloc : gqa::Layout<D>::kAlloc;
+    const int threads = persistent ? gqa::kWsThreads : gqa::kThreads;
+    if (persistent) kid += 8;
+    unsigned grid;
+    if (persistent) {
+        const int sms = g_dev_sms[dev];
+        grid = static_cast<unsigned>(prm.n_items < sms ? prm.n_items : sms);
+    } else {
+        grid = static_cast<unsigned>(static_cast<long long>(prm.BHq) * prm.n_qtiles);
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!(g_dev_smem_set[dev] >> kid & 1u)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) {
+                note_cuda_error(e, "cudaFuncSetAttribute");
+                return ATTN_ERR_LAUNCH;
+            }
+            g_dev_smem_set[dev] |= 1u << kid;
+        }
+    }
+    kern<<<grid, threads, smem, stream>>>(tq, tk, tv, prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "kernel launch");
+        return ATTN_ERR_LAUNCH;
+    }
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                       int Hkv, int N, int D, float scale, int causal, attn_dtype_t dtype, void *stream) {
+    if (B < 0 || Hq < 0 || N < 0 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_SHAPE;
+    if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+    if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+    if (B == 0 || Hq == 0 || N == 0) return ATTN_OK;
+    if (!q || !k || !v || !o) return ATTN_ERR_NULL;
+    auto misaligned = [](const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+        (lse && misaligned(lse, 4)))
+        return ATTN_ERR_ALIGN;
+    const long long BHq = static_cast<long long>(B) * Hq;
+    const long long BHkv = static_cast<long long>(B) * Hkv;
+    const int n_tiles = (N + gqa::kBN - 1) / gqa::kBN;
+    if (BHq * n_tiles > INT_MAX) return ATTN_ERR_SHAPE;
+
+    int dev = 0;
+    attn_status_t st = check_device(&dev);
+    if (st != ATTN_OK) return st;
+
+    const bool bf16 = dtype == ATTN_BF16;
+    CUtensorMap tq, tk, tv;
+    if (!encode_qkv_map(&tq, q, bf16, D, N, BHq) || !encode_qkv_map(&tk, k, bf16, D, N, BHkv) ||
+        !encode_qkv_map(&tv, v, bf16, D, N, BHkv)) {
+        std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
+        return ATTN_ERR_LAUNCH;
+    }
+    gqa::Params prm;
+    prm.o = o;
+    prm.lse = lse;
+    prm.N = N;
+    prm.group = Hq / Hkv;
+    prm.n_qtiles = n_tiles;
+    prm.n_kv_tiles = n_tiles;
+    prm.BHq = static_cast<int>(BHq);
+    prm.n_qblocks = (N + 255) / 256;
+    prm.n_items = static_cast<int>(BHq * prm.n_qblocks);
+    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    prm.seq = g_launch_seq.fetch_add(1);
+    prm.timeout_ns = g_timeout_ns.load();
+    prm.inject_stall = g_inject_stall.load();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+    switch (kid) {
+        case 0: return launch<64, false, false>(dev, kid, tq, tk, tv, prm, s);
+        case 1: return launch<64, false, true>(dev, kid, tq, tk, tv, prm, s);
+        case 2: return launch<64, true, false>(dev, kid, tq, tk, tv, prm, s);
+        case 3: return launch<64, true, true>(dev, kid, tq, tk, tv, prm, s);
+        case 4: return launch<128, false, false>(dev, kid, tq, tk, tv, prm, s);
+        case 5: return launch<128, false, true>(dev, kid, tq, tk, tv, prm, s);
+        case 6: return launch<128, true, false>(dev, kid, tq, tk, tv, prm, s);
+        default: return launch<128, true, true>(dev, kid, tq, tk, tv, prm, s);
+    }
+}
+
+const char *attn_status_str(attn_status_t status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_NULL: return "null pointer";
+        case ATTN_ERR_SHAPE: return "invalid shape or scale";
+        case ATTN_ERR_HEADDIM: return "unsupported head dimension (64 or 128)";
+        case ATTN_ERR_DTYPE: return "unsupported dtype";
+        case ATTN_ERR_ALIGN: return "misaligned pointer";
+        case ATTN_ERR_LAUNCH: return "CUDA launch or driver call failed";
+        case ATTN_ERR_TIMEOUT: return "in-kernel wait timed out";
+        case ATTN_ERR_NODEVICE: return "no sm_103 device is current";
+    }
+    return "unknown status";
+}
+
+attn_status_t attn_last_device_error(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaStreamSynchronize");
+        return ATTN_ERR_LAUNCH;
+    }
+    int code = 0;
+    e = cudaMemcpyFromSymbol(&code, gqa::g_error_code, sizeof(int));
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaMemcpyFromSymbol");
+        return ATTN_ERR_LAUNCH;
+    }
+    if (code != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(gqa::g_error_code, &zero, sizeof(int));
+        if (e != cudaSuccess) note_cuda_error(e, "cudaMemcpyToSymbol");
+    }
+    return static_cast<attn_status_t>(code);
+}
+
+const char *attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int attn_version(void) { return 0x000100; }
+
+void attn_test_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : 4000000000ull); }
+
+void attn_test_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+
+void attn_test_select_kernel(int which) { g_kernel_choice.store(which == 1 ? 1 : 0); }
+
+}  // extern "C"

@@ -1,0 +1,414 @@
+// Persistent, warp-specialised fused GQA attention forward for sm_103a.
+//
+// A work item is a 256-row query block of one (batch, query head): two
+// 128-row query tiles Q0, Q1 that share every K/V tile the producer brings
+// in.  The online-softmax update is the one of the page "从零开始写Qwen3"
+// (deepseek.csdn.net/6a3201f8..., sections "在线softmax" and "FlashAttention").
+//
+// Roles (384 threads):
+//   warp 0        TMA producer: Q0, K_0, Q1, V_0, K_1, V_1, ... into a ring of
+//                 kStagesWs 128-byte-swizzled tiles (full / empty mbarriers).
+//   warp 1        MMA issuer (one lane):  S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per
+//                 key tile j:  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,
+//                 S1 = Q1 K_{j+1}^T.  While softmax warpgroup 0 works on S0 the
+//                 tensor core runs tile 1's products, and the other way round.
+//   warps 4-7     softmax warpgroup 0 (rows of Q0, one row per thread = TMEM lane)
+//   warps 8-11    softmax warpgroup 1 (rows of Q1)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// P_i (the probabilities, rounded to the input type, two per 32-bit column)
+// overwrites the first 64 columns of S_i and is the TMEM A operand of P_i V_j,
+// so P never goes through shared memory.  The commit that signals S_i(j+1)
+// also covers P_i V_j (tcgen05.commit tracks every earlier MMA), so when a
+// softmax thread sees S_i(j+1) its O_i row is stable and can be rescaled.
+//
+// Work items are ordered longest causal row block first and dealt to the
+// persistent CTAs in a snake order (CTA c takes item r*G + c on even rounds and
+// r*G + G-1-c on odd rounds), which evens out the linearly shrinking causal
+// work; the heads of one GQA group are adjacent so their K/V reads share L2
+// (page "从零开始写Qwen3", deepseek.csdn.net/6a31faef..., "改进1-使用正确的grid").
+// Causal tiles above the diagonal are never loaded and only diagonal tiles are
+// masked (same page, "改进2-KV只读取下三角", "改进3-两阶段计算").
+#pragma once
+#include "kernel_common.cuh"
+
+namespace gqa {
+
+constexpr int kWsThreads = 384;
+constexpr int kStagesWs = 4;
+constexpr uint32_t kWsTmemCols = 512;
+constexpr uint32_t kRegsLow = 88;   // warps 0-3 after the hand-off
+constexpr uint32_t kRegsHigh = 208;  // softmax warpgroups after the hand-off (128*88 + 256*208 = 384*168)
+
+template <int D>
+struct WsLayout {
+    static constexpr int kAtoms = D / 64;
+    static constexpr int kAtomBytes = 128 * 128;  // 128 rows x 128 B
+    static constexpr int kTileBytes = kAtoms * kAtomBytes;
+    static constexpr int kQ = 0;  // Q0, Q1
+    static constexpr int kKV = kQ + 2 * kTileBytes;
+    static constexpr int kBar = kKV + kStagesWs * kTileBytes;
+    // q_full[2], q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], mma_done
+    static constexpr int kNumBars = 2 + 1 + 2 * kStagesWs + 2 + 2 + 2 + 1;
+    static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 4;
+    static constexpr int kUsed = kAbort + 4;
+    // at least half of the SM's shared memory, so that one CTA (which takes all
+    // 512 TMEM columns) is resident per SM
+    static constexpr int kAlloc = (kUsed + 1024) > 118 * 1024 ? (kUsed + 1024) : 118 * 1024;
+};
+
+// Position in the K/V ring.
+struct Ring {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next() {
+        if (++s == kStagesWs) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Work item of round r for this CTA (snake order), or false past the end.
+__device__ __forceinline__ bool ws_item(const Params &p, int r, int &bh, int &qb) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = (r & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    const long long t = static_cast<long long>(r) * G + c;
+    if (t >= p.n_items) return false;
+    qb = p.n_qblocks - 1 - static_cast<int>(t / p.BHq);
+    bh = static_cast<int>(t % p.BHq);
+    return true;
+}
+
+// Key tiles visited by query tile i (0, 1) of block qb.
+template <bool kCausal>
+__device__ __forceinline__ int ws_tiles(const Params &p, int qb, int i) {
+    if (!kCausal) return p.n_kv_tiles;
+    const int n = 2 * qb + 1 + i;  // up to and including the diagonal tile
+    return n < p.n_kv_tiles ? n : p.n_kv_tiles;
+}
+
+template <int D, bool kBF16, bool kCausal>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using L = WsLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t sQ = base + L::kQ, sKV = base + L::kKV;
+    const uint32_t bar0 = base + L::kBar;
+    auto q_full = [&](int i) { return bar0 + 8u * i; };
+    const uint32_t q_empty = bar0 + 8u * 2;
+    auto kv_full = [&](int s) { return bar0 + 8u * (3 + s); };
+    auto kv_empty = [&](int s) { return bar0 + 8u * (3 + kStagesWs + s); };
+    auto s_full = [&](int i) { return bar0 + 8u * (3 + 2 * kStagesWs + i); };
+    auto p_full = [&](int i) { return bar0 + 8u * (5 + 2 * kStagesWs + i); };
+    auto o_full = [&](int i) { return bar0 + 8u * (7 + 2 * kStagesWs + i); };
+    const uint32_t mma_done = bar0 + 8u * (9 + 2 * kStagesWs);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
+        mbar_init(q_full(0), 1);
+        mbar_init(q_full(1), 1);
+        mbar_init(q_empty, 1);
+        for (int s = 0; s < kStagesWs; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full(i), 1);
+            mbar_init(p_full(i), 128);
+            mbar_init(o_full(i), 1);
+        }
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (*abort_flag) return;  // another CTA of this launch already gave up
+    if (warp == 1) {
+        tmem_alloc(base + L::kTmemSlot, kWsTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        regs_dec<kRegsLow>();
+        if (warp == 0 && lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            Ring ring;
+            uint32_t used = 0, last_phase = 0;
+            int items = 0;
+            bool ok = true;
+            auto load_kv = [&](const void *tm, int row, int kvh) -> bool {
+                if (!wait_bar(kv_empty(ring.s), ring.ph ^ 1u, p, abort_flag)) return false;
+                mbar_arrive_expect_tx(kv_full(ring.s), L::kTileBytes);
+#pragma unroll
+                for (int a = 0; a < L::kAtoms; ++a)
+                    tma_load_3d(sKV + ring.s * L::kTileBytes + a * L::kAtomBytes, tm, a * 64, row, kvh,
+                                kv_full(ring.s));
+                used |= 1u << ring.s;
+                last_phase = (last_phase & ~(1u << ring.s)) | (ring.ph << ring.s);
+                ring.next();
+                return true;
+            };
+            for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
+                int bh, qb;
+                if (!ws_item(p, r, bh, qb)) continue;
+                const int kvh = bh / p.group;
+                const int q0 = qb * 256;
+                const int n1 = ws_tiles<kCausal>(p, qb, 1);
+                // K_0 may land while the previous item still runs; the Q buffers
+                // are free once every S MMA of the previous item is done.
+                if (!load_kv(&tmK, 0, kvh)) break;
+                if (!wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag)) break;
+                if (!p.inject_stall) {
+                    mbar_arrive_expect_tx(q_full(0), L::kTileBytes);
+#pragma unroll
+                    for (int a = 0; a < L::kAtoms; ++a)
+                        tma_load_3d(sQ + a * L::kAtomBytes, &tmQ, a * 64, q0, bh, q_full(0));
+                    mbar_arrive_expect_tx(q_full(1), L::kTileBytes);
+#pragma unroll
+                    for (int a = 0; a < L::kAtoms; ++a)
+                        tma_load_3d(sQ + L::kTileBytes + a * L::kAtomBytes, &tmQ, a * 64, q0 + 128, bh,
+                                    q_full(1));
+                }
+                ++items;
+                for (int j = 0; j < n1 && ok; ++j) {
+                    ok = load_kv(&tmV, j * kBN, kvh);
+                    if (ok && j + 1 < n1) ok = load_kv(&tmK, (j + 1) * kBN, kvh);
+                }
+            }
+            // Every copy issued must have landed before the CTA may exit.
+            if (items > 0 && !p.inject_stall) {
+                drain_bar(q_full(0), (items - 1) & 1, p);
+                drain_bar(q_full(1), (items - 1) & 1, p);
+            }
+            for (int s = 0; s < kStagesWs; ++s)
+                if (used >> s & 1u) drain_bar(kv_full(s), last_phase >> s & 1u, p);
+        } else if (warp == 1 && lane == 0) {
+            // ---------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, 128, kBN, false);
+            constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, 128, D, true);
+            Ring ring;
+            uint32_t pcount[2] = {0, 0};
+            int items = 0;
+            bool ok = true;
+            auto qk = [&](int i, int kstage) {
+                const uint32_t a0 = sQ + i * L::kTileBytes, b0 = sKV + kstage * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+                    mma_f16_ss(tmem + 128u * i, sdesc_sw128(a0 + off, 16, 1024),
+                               sdesc_sw128(b0 + off, 16, 1024), idesc_qk, kk > 0);
+                }
+            };
+            auto pv = [&](int i, int vstage, bool acc) {
+                const uint32_t b0 = sKV + vstage * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_f16_ts(tmem + 256u + 128u * i, tmem + 128u * i + 8u * kk,
+                               sdesc_sw128(b0 + kk * 2048, L::kAtomBytes, 1024), idesc_pv,
+                               (acc || kk > 0) ? 1u : 0u);
+            };
+            for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
+                int bh, qb;
+                if (!ws_item(p, r, bh, qb)) continue;
+                const int n0 = ws_tiles<kCausal>(p, qb, 0), n1 = ws_tiles<kCausal>(p, qb, 1);
+                const uint32_t ip = items & 1;
+                if (!(ok = wait_bar(q_full(0), ip, p, abort_flag))) break;
+                if (!(ok = wait_bar(kv_full(ring.s), ring.ph, p, abort_flag))) break;
+                tc_fence_after();
+                qk(0, ring.s);
+                mma_commit(s_full(0));
+                if (!(ok = wait_bar(q_full(1), ip, p, abort_flag))) break;
+                tc_fence_after();
+                qk(1, ring.s);
+                mma_commit(s_full(1));
+                mma_commit(kv_empty(ring.s));
+                ring.next();
+                for (int j = 0; j < n1; ++j) {
+                    const int vs = ring.s;
+                    if (!(ok = wait_bar(kv_full(vs), ring.ph, p, abort_flag))) break;
+                    ring.next();
+                    if (j < n0) {
+                        if (!(ok = wait_bar(p_full(0), pcount[0] & 1u, p, abort_flag))) break;
+                        ++pcount[0];
+                        tc_fence_after();
+                        pv(0, vs, j > 0);
+                        if (j == n0 - 1) mma_commit(o_full(0));
+                    }
+                    const bool more = j + 1 < n1;
+                    const int ks = ring.s;
+                    if (more) {
+                        if (!(ok = wait_bar(kv_full(ks), ring.ph, p, abort_flag))) break;
+                        tc_fence_after();
+                        if (j + 1 < n0) {
+                            qk(0, ks);
+                            mma_commit(s_full(0));
+                        }
+                    }
+                    if (!(ok = wait_bar(p_full(1), pcount[1] & 1u, p, abort_flag))) break;
+                    ++pcount[1];
+                    tc_fence_after();
+                    pv(1, vs, j > 0);
+                    if (j == n1 - 1) mma_commit(o_full(1));
+                    mma_commit(kv_empty(vs));
+                    if (more) {
+                        qk(1, ks);
+                        mma_commit(s_full(1));
+                        mma_commit(kv_empty(ks));
+                        ring.next();
+                    }
+                }
+                if (!ok) break;
+                mma_commit(q_empty);  // this item's S MMAs no longer read Q0, Q1
+                ++items;
+            }
+            // TMEM and shared memory stay alive until every issued MMA is done.
+            mma_commit(mma_done);
+            drain_bar(mma_done, 0, p);
+        }
+        __syncwarp();
+    } else {
+        regs_inc<kRegsHigh>();
+        // -------------------------------------------------------- softmax
+        const int i = (warp - 4) >> 2;  // query tile of this warpgroup
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // row within the tile == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + 128u * i + lane_off;  // S_i, and P_i in its first 64 columns
+        const uint32_t tO = tmem + 256u + 128u * i + lane_off;
+        const float c = p.scale_log2;
+        uint32_t scount = 0;
+        int items = 0;
+        bool ok = true;
+        for (int rr = 0; ok && static_cast<long long>(rr) * gridDim.x < p.n_items; ++rr) {
+            int bh, qb;
+            if (!ws_item(p, rr, bh, qb)) continue;
+            const int n = ws_tiles<kCausal>(p, qb, i);
+            const int row0 = qb * 256 + 128 * i;  // first query row of this tile
+            const int diag = row0 / kBN;           // causal: the one masked key tile
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < n; ++j) {
+                if (!__all_sync(0xffffffffu, wait_bar(s_full(i), scount & 1u, p, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                ++scount;
+                tc_fence_after();
+                __syncwarp();
+                uint32_t s[128];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld32(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q]));
+                tmem_ld_wait(s);
+                if (kCausal) {
+                    if (j == diag) {  // keep key c <= row r
+#pragma unroll
+                        for (int cc = 0; cc < 128; ++cc)
+                            if (cc > r) s[cc] = __float_as_uint(-INFINITY);
+                    }
+                } else if ((j + 1) * kBN > p.N) {  // ragged last tile: keys >= N are absent
+                    const int lim = p.N - j * kBN;
+#pragma unroll
+                    for (int cc = 0; cc < 128; ++cc)
+                        if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
+                }
+                float mx[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) mx[t] = u2f(s[t]);
+#pragma unroll
+                for (int cc = 8; cc < 128; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], u2f(s[cc]));
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float m_new = fmaxf(m, mt);
+                const float alpha = ex2_approx((m - m_new) * c);  // 0 on the first tile
+                if (j > 0 && __any_sync(0xffffffffu, m_new > m)) {
+                    // O_i holds P_i V_{j-1} already (covered by the S_i(j) commit).
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * q, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(u2f(o[t]) * alpha);
+                        tmem_st32(tO + 32 * q, o);
+                    }
+                }
+                m = m_new;
+                const float mc = m * c;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const float e0 = ex2_approx(fmaf(u2f(s[64 * q + 2 * t]), c, -mc));
+                        const float e1 = ex2_approx(fmaf(u2f(s[64 * q + 2 * t + 1]), c, -mc));
+                        ls[(2 * t) & 3] += e0;
+                        ls[(2 * t + 1) & 3] += e1;
+                        pk[t] = pack2<kBF16>(e0, e1);
+                    }
+                    tmem_st32(tS + 32 * q, pk);
+                }
+                l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_full(i));
+            }
+            if (!ok) break;
+            // ---------------------------------------------------- epilogue
+            if (!__all_sync(0xffffffffu, wait_bar(o_full(i), items & 1, p, abort_flag))) {
+                ok = false;
+                break;
+            }
+            ++items;
+            tc_fence_after();
+            __syncwarp();
+            const int row = row0 + r;
+            const float inv_l = 1.f / l;
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.N + row) * (D * 2);
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * q, o);
+                tmem_ld_wait(o);
+                if (row < p.N) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        w[t] = pack2<kBF16>(u2f(o[2 * t]) * inv_l, u2f(o[2 * t + 1]) * inv_l);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        st_global_v4(orow + q * 64 + v * 16, w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                                     w[4 * v + 3]);
+                }
+            }
+            if (p.lse != nullptr && row < p.N)
+                p.lse[static_cast<size_t>(bh) * p.N + row] = (m * c + log2f(l)) * 0.6931471805599453f;
+            // O_i is read; the next item's first P_i V MMA waits for this warpgroup's p_full.
+            tc_fence_before();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kWsTmemCols);
+    }
+}
+
+}  // namespace gqa

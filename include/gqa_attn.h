@@ -1,0 +1,126 @@
+/*
+ * gqa_attn.h -- C ABI of the GB300 (sm_103a) fused grouped-query attention
+ * forward library (libgqa_attn.so).
+ *
+ * The operation is the fused attention forward of the page "从零开始写Qwen3"
+ * (deepseek.csdn.net/6a3201f8..., section "FlashAttention": O_i is the sum over
+ * key blocks j of softmax(mask(Q_i K_j^T / sqrt(D))) V_j, computed with the
+ * online-softmax update of section "在线softmax" so that no N x N score matrix
+ * is ever stored), with
+ *   - grouped-query heads: query head hq reads key/value head
+ *     hq / (Hq / Hkv) of the same batch entry (same section's kernel: the
+ *     flattened (b, q_head) index divided by the group count);
+ *   - the optional causal mask j <= i on absolute row indices (same section:
+ *     positions with offsets_qm >= offsets_kk are kept);
+ *   - the natural-log log-sum-exp of each masked, scaled score row,
+ *     lse = max_j s_ij + ln(sum_j exp(s_ij - max_j s_ij)), written as fp32.
+ *
+ * Arithmetic: Q K^T and P V on the tensor cores with fp32 accumulation;
+ * running max, running sum and the output accumulator in fp32 (page
+ * "从零开始写Qwen3", deepseek.csdn.net/6a31faef..., section "改进点4-去掉多余的
+ * 转换"); the probabilities P are rounded to the input type before the P V
+ * product; O is rounded once, to nearest even, at the end.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and o. */
+typedef enum {
+    ATTN_F16 = 0,  /* IEEE binary16 */
+    ATTN_BF16 = 1  /* bfloat16 */
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,     /* q, k, v or o is NULL while the problem is non-empty */
+    ATTN_ERR_SHAPE = 2,    /* negative size, Hkv < 1, Hq % Hkv != 0, a size too
+                              large for 32-bit tile coordinates, or scale not
+                              finite and > 0 */
+    ATTN_ERR_HEADDIM = 3,  /* D is not 64 or 128 */
+    ATTN_ERR_DTYPE = 4,    /* dtype is not ATTN_F16 / ATTN_BF16 */
+    ATTN_ERR_ALIGN = 5,    /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+    ATTN_ERR_LAUNCH = 6,   /* a CUDA runtime / driver call failed (see attn_last_cuda_error) */
+    ATTN_ERR_TIMEOUT = 7,  /* a bounded in-kernel wait ran out (reported by
+                              attn_last_device_error) */
+    ATTN_ERR_NODEVICE = 8  /* no CUDA device of compute capability 10.3 is current */
+} attn_status_t;
+
+/*
+ * attn_fwd -- O = softmax(mask(Q K^T * scale)) V and LSE, one kernel launch.
+ *
+ * q    device pointer, [B, Hq,  N, D] contiguous (row-major, D fastest), dtype
+ * k    device pointer, [B, Hkv, N, D] contiguous, dtype
+ * v    device pointer, [B, Hkv, N, D] contiguous, dtype
+ * o    device pointer, [B, Hq,  N, D] contiguous, dtype (written)
+ * lse  device pointer, [B, Hq, N] fp32 (written), or NULL to skip it
+ * B, Hq, Hkv, N   batch, query heads, key/value heads (Hq % Hkv == 0), sequence
+ *                 length (keys and queries have the same length N)
+ * D      head dimension, 64 or 128
+ * scale  logit scale, finite and > 0 (1/sqrt(D) for standard attention)
+ * causal nonzero: keep only keys j <= i for query row i (top-left aligned)
+ * dtype  ATTN_F16 or ATTN_BF16 for q, k, v and o
+ * stream CUDA stream (cudaStream_t) the kernel is launched on; NULL = legacy
+ *        default stream
+ *
+ * Ownership: the caller owns every buffer; the library allocates no device
+ * memory per call and keeps no pointer after the call returns.  o must not
+ * overlap q, k or v.
+ * Asynchrony: returns after the launch is queued on `stream`; results are
+ * ready when the stream reaches that point.
+ * Errors: argument errors are returned before anything is launched and leave
+ * o and lse untouched.  An empty problem (B, Hq or N equal to 0) launches
+ * nothing and returns ATTN_OK.  A wait inside the kernel that runs out of time
+ * makes the kernel stop early and record ATTN_ERR_TIMEOUT, which
+ * attn_last_device_error reports; o and lse are then undefined.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                       attn_dtype_t dtype, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *attn_status_str(attn_status_t status);
+
+/*
+ * Synchronises `stream`, then returns and clears the error word that kernels
+ * of this library set on the current device (ATTN_OK if none).  A CUDA error
+ * raised by the synchronisation itself is returned as ATTN_ERR_LAUNCH.
+ */
+attn_status_t attn_last_device_error(void *stream);
+
+/* Text of the last CUDA error this library saw on the calling thread ("" if none). */
+const char *attn_last_cuda_error(void);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int attn_version(void);
+
+/*
+ * Test hooks for the failure path (process-wide, affect later launches).
+ *
+ * attn_test_set_wait_timeout_ns: limit of every bounded in-kernel wait, in
+ *   nanoseconds; 0 restores the default (4 s).
+ * attn_test_inject_stall: nonzero makes later launches skip the load of the
+ *   query tile, so the MMA warp's wait on it can only end by running out; the
+ *   kernel then records ATTN_ERR_TIMEOUT, drains its own copies in flight,
+ *   frees its TMEM and returns.  0 restores normal launches.
+ * Neither hook faults, traps or hangs the GPU.
+ */
+void attn_test_set_wait_timeout_ns(unsigned long long ns);
+void attn_test_inject_stall(int enable);
+
+/*
+ * attn_test_select_kernel: 0 (default) = persistent warp-specialised kernel
+ *   (two 128-row query tiles per work item, P kept in TMEM); 1 = the simpler
+ *   kernel with one CTA per 128-row query tile and P staged in shared memory.
+ *   Both compute the same operation; the second exists to cross-check the first.
+ */
+void attn_test_select_kernel(int which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for sm_103a,
+loads, exports every symbol the header declares, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gqa_attention_forward_gb300 import binding, build
+
+HEADER = os.path.join(build.INCLUDE, "gqa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w \*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["attn_fwd", "attn_status_str", "attn_last_device_error", "attn_last_cuda_error",
+              "attn_version", "attn_test_set_wait_timeout_ns", "attn_test_inject_stall"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gqa_attn.h but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        s = binding.attn_status_str(code)
+        assert s and s != "unknown status", name
+    assert binding.attn_status_str(99) == "unknown status"
+    assert binding.attn_version() == 0x000100
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(Hkv=0), 2), (dict(Hq=6, Hkv=4), 2), (dict(N=-1), 2), (dict(B=-2), 2),
+    (dict(scale=0.0), 2), (dict(scale=float("inf")), 2), (dict(scale=float("nan")), 2),
+    (dict(D=96), 3), (dict(D=256), 3), (dict(dtype=7), 4),
+    (dict(q=0), 1), (dict(o=0), 1), (dict(q=FAKE + 8), 5), (dict(v=FAKE + 2), 5),
+    (dict(lse=FAKE + 2), 5),
+])
+def test_argument_errors(lib, args, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=4, Hkv=2, N=16, D=128, scale=0.1,
+             causal=1, dtype=1)
+    a.update(args)
+    st = binding.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                          a["N"], a["D"], a["scale"], a["causal"], a["dtype"], None)
+    assert st == code, (args, binding.STATUS.get(st))
+
+
+@pytest.mark.parametrize("empty", [dict(B=0), dict(Hq=0), dict(N=0)])
+def test_empty_problem_is_a_no_op(lib, empty):
+    a = dict(B=1, Hq=4, Hkv=2, N=16)
+    a.update(empty)
+    st = binding.attn_fwd(None, None, None, None, None, a["B"], a["Hq"], a["Hkv"], a["N"], 128,
+                          0.1, 1, 1, None)
+    assert st == 0
+
+
+def test_no_device_is_reported_without_a_gpu(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this checks the no-device path")
+    st = binding.attn_fwd(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 16, 128, 0.1, 1, 1, None)
+    assert st == 8  # ATTN_ERR_NODEVICE: validated, then refused before any launch
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load(str(tmp_path / "libgqa_attn.so"))
+
+
+def test_oracle_is_not_on_the_product_path():
+    pkg = os.path.dirname(binding.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", text, flags=re.M), f
+                assert "attn_oracle" not in text, f
+
+
+def test_ctypes_signature_matches_header(lib):
+    assert lib.attn_fwd.restype is ctypes.c_int
+    assert len(lib.attn_fwd.argtypes) == 14

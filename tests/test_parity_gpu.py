@@ -1,0 +1,205 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle."""
+import zlib
+
+import numpy as np
+import pytest
+
+from gqa_attention_forward_gb300 import binding, workloads
+from parity_util import assert_parity, oracle_full, oracle_rows, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return t.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny_causal_gqa_f16", "pages_shape_causal_gqa_f16"])
+def test_workload_full(name):
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    o, lse = run_gpu(w, x)
+    ro, rl = oracle_full(w, x)
+    err = assert_parity(w, _np(o), _np(lse), ro, rl, name)
+    print(f"{name}: max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
+
+
+def test_tail_stress_every_row():
+    """N = 2000 (ragged last tile), logits with std 16: every row against the oracle."""
+    w = workloads.WORKLOADS["tail_stress_causal_gqa_bf16_n2000"]
+    x = workloads.make_inputs(w)
+    o, lse = run_gpu(w, x)
+    ro, rl = oracle_full(w, x)
+    err = assert_parity(w, _np(o), _np(lse), ro, rl, w.name)
+    print(f"{w.name}: max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
+
+
+@pytest.mark.parametrize("name,count", [("noncausal_gqa_bf16_n4096", 3000),
+                                        ("long_prefill_causal_gqa_bf16_n32768", 1500)])
+def test_workload_sampled_rows(name, count):
+    """Full-size launch (the benchmarked configuration); oracle on a stratified row sample."""
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    o, lse = run_gpu(w, x)
+    rows = workloads.sample_rows(w, count)
+    og = _np(o).reshape(-1, w.D)[rows]
+    lg = _np(lse).reshape(-1)[rows]
+    ro, rl = oracle_rows(w, x, rows)
+    err = assert_parity(w, og, lg, ro, rl, name)
+    print(f"{name}: {len(rows)} rows max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
+    # properties that hold at any size, checked on every row
+    assert np.all(np.isfinite(_np(lse)))
+    assert np.all(np.isfinite(_np(o)))
+
+
+SHAPES = [
+    # B, Hq, Hkv, N, D, dtype, causal, qk_std
+    (1, 1, 1, 1, 64, "f16", True, 1.0),
+    (1, 1, 1, 1, 128, "bf16", False, 1.0),
+    (1, 2, 1, 2, 64, "bf16", True, 1.0),
+    (2, 4, 2, 63, 128, "f16", True, 1.0),
+    (2, 4, 2, 63, 128, "f16", False, 1.0),
+    (1, 8, 2, 127, 64, "bf16", False, 1.0),
+    (1, 8, 2, 128, 128, "bf16", True, 1.0),
+    (1, 4, 1, 129, 128, "f16", False, 1.0),
+    (1, 4, 1, 129, 128, "bf16", True, 4.0),
+    (3, 6, 3, 200, 64, "f16", True, 1.0),
+    (1, 8, 8, 257, 128, "bf16", False, 4.0),
+    (2, 8, 1, 384, 128, "f16", True, 1.0),
+    (1, 2, 2, 1000, 64, "bf16", True, 1.0),
+    (1, 16, 4, 640, 128, "bf16", False, 1.0),
+    (1, 4, 4, 1024, 128, "f16", False, 1.0),
+    (2, 2, 1, 1500, 64, "f16", False, 2.0),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_random_shapes(shape):
+    B, Hq, Hkv, N, D, dtype, causal, std = shape
+    w = workloads.Workload("rand", B, Hq, Hkv, N, D, dtype, causal, q_std=std, k_std=std,
+                           seed=zlib.crc32(repr(shape).encode()) & 0xFFFF)
+    x = workloads.make_inputs(w)
+    o, lse = run_gpu(w, x)
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o), _np(lse), ro, rl, str(shape))
+
+
+def test_no_writes_past_the_outputs():
+    """Rows >= N of the last tile are never stored: canaries after O and LSE survive."""
+    import torch
+
+    w = workloads.Workload("canary", 1, 4, 2, 200, 128, "bf16", False, seed=7)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    n_o = w.B * w.Hq * w.N * w.D
+    o_buf = torch.full((n_o + 4096,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((w.B * w.Hq * w.N + 1024,), -777.0, dtype=torch.float32, device="cuda")
+    o = o_buf[:n_o].view(w.B, w.Hq, w.N, w.D)
+    lse = l_buf[: w.B * w.Hq * w.N].view(w.B, w.Hq, w.N)
+    binding.attention(q, k, v, causal=w.causal, scale=w.scale, out=o, lse_out=lse)
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[n_o:] == 12345.0)
+    assert torch.all(l_buf[w.B * w.Hq * w.N:] == -777.0)
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "canary")
+
+
+def test_lse_optional_and_deterministic():
+    import torch
+
+    w = workloads.Workload("nolse", 2, 8, 2, 300, 128, "f16", True, seed=11)
+    x = workloads.make_inputs(w)
+    o1, lse = run_gpu(w, x)
+    o2, none = run_gpu(w, x, with_lse=False)
+    assert none is None
+    assert torch.equal(o1, o2)
+
+
+def test_side_stream():
+    import torch
+
+    w = workloads.Workload("stream", 1, 4, 1, 256, 64, "bf16", True, seed=12)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        o, lse = binding.attention(q, k, v, causal=True, scale=w.scale, stream=s)
+    assert binding.attn_last_device_error(s) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "side stream")
+
+
+def test_timeout_is_reported_and_context_survives():
+    """A wait that nothing can satisfy runs out: the kernel records ATTN_ERR_TIMEOUT,
+    drains its copies, frees TMEM and returns; the next launch is correct."""
+    import torch
+
+    lib = binding.load()
+    w = workloads.Workload("stall", 1, 2, 1, 512, 128, "bf16", True, seed=13)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    try:
+        lib.attn_test_set_wait_timeout_ns(300_000_000)
+        lib.attn_test_inject_stall(1)
+        binding.attention(q, k, v, causal=True, scale=w.scale)
+        st = binding.attn_last_device_error(torch.cuda.current_stream())
+    finally:
+        lib.attn_test_inject_stall(0)
+        lib.attn_test_set_wait_timeout_ns(0)
+    assert st == binding.ATTN_ERR_TIMEOUT
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    o, lse = binding.attention(q, k, v, causal=True, scale=w.scale)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "after timeout")
+
+
+def test_scale_is_honoured():
+    import torch
+
+    from oracle import attention, widen
+
+    w = workloads.Workload("scale", 1, 2, 1, 160, 64, "f16", False, seed=14)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o, lse = binding.attention(q, k, v, causal=False, scale=0.05)
+    torch.cuda.synchronize()
+    ro, rl, _ = attention(widen(x["q"], "f16"), widen(x["k"], "f16"), widen(x["v"], "f16"), 0.05, False)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "scale 0.05")
+
+
+@pytest.fixture
+def tile_kernel():
+    """Selects the one-CTA-per-query-tile kernel for the test, then restores the default."""
+    lib = binding.load()
+    lib.attn_test_select_kernel(1)
+    yield
+    lib.attn_test_select_kernel(0)
+
+
+@pytest.mark.parametrize("shape", SHAPES[::2], ids=lambda s: "x".join(map(str, s)))
+def test_tile_kernel_random_shapes(shape, tile_kernel):
+    test_random_shapes(shape)
+
+
+def test_tile_kernel_timeout(tile_kernel):
+    test_timeout_is_reported_and_context_survives()
+
+
+def test_both_kernels_agree_on_pages_shape():
+    """The two kernels compute the same function; their outputs differ by rounding only."""
+    import torch
+
+    lib = binding.load()
+    w = workloads.WORKLOADS["pages_shape_causal_gqa_f16"]
+    x = workloads.make_inputs(w)
+    o1, l1 = run_gpu(w, x)
+    try:
+        lib.attn_test_select_kernel(1)
+        o2, l2 = run_gpu(w, x)
+    finally:
+        lib.attn_test_select_kernel(0)
+    assert float((o1.float() - o2.float()).abs().max()) <= 2e-3
+    assert float((l1 - l2).abs().max()) <= 1e-4 * max(1.0, float(l1.abs().max()))
+    assert torch.isfinite(o1).all()
