@@ -8,9 +8,9 @@
 // end.  The score matrix never leaves the SM.
 //
 // Hardware mapping:
-//   * warp 0 (one lane): TMA producer.  Q once; then K_j, V_j alternately into
-//     a kStages-deep ring of 128-byte-swizzled shared-memory tiles guarded by
-//     full / empty mbarriers.
+//   * warps 2-3: loaders.  Q once; then K_j, V_j alternately, with 16-byte
+//     cp.async into a kStages-deep ring of 128-byte-swizzled shared-memory
+//     tiles guarded by full / empty mbarriers.
 //   * warp 1 (one lane): tcgen05 MMA issuer.  S = Q K_j^T into TMEM columns
 //     [0, 128); O += P V_j into TMEM columns [128, 128 + D).  Completion is
 //     signalled with tcgen05.commit onto mbarriers.
@@ -47,14 +47,13 @@
 namespace gqa {
 
 constexpr int kStages = 4;     // K/V tiles in flight
-constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 4..7 softmax
+constexpr int kThreads = 256;  // warps 2-3 loaders, warp 1 MMA, warps 4..7 softmax
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemO = 128;  // first TMEM column of the O accumulator
 
 template <int D>
 struct Layout {
     static constexpr int kAtoms = D / 64;           // 64 halfs = one 128-byte swizzle row
-    static constexpr int kAtomBytes = 128 * 128;    // 128 rows x 128 B
     static constexpr int kTileBytes = kAtoms * kAtomBytes;
     static constexpr int kQ = 0;
     static constexpr int kKV = kQ + kTileBytes;
@@ -70,8 +69,7 @@ struct Layout {
 
 template <int D, bool kBF16, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+    attn_fwd_kernel(const Params p) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -100,9 +98,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
-        mbar_init(q_full, 1);
+        mbar_init(q_full, kLoaderThreads);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(kv_full(s), 1);
+            mbar_init(kv_full(s), kLoaderThreads);
             mbar_init(kv_empty(s), 1);
         }
         mbar_init(s_full, 1);
@@ -122,51 +120,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            bool issued_q = false;
-            if (!p.inject_stall) {
-                mbar_arrive_expect_tx(q_full, L::kTileBytes);
-#pragma unroll
-                for (int a = 0; a < L::kAtoms; ++a)
-                    tma_load_3d(sQ + a * L::kAtomBytes, &tmQ, a * 64, q0, bh, q_full);
-                issued_q = true;
-            }
-            int stage = 0;
-            uint32_t phase = 0, used = 0, last_phase = 0;
-            bool ok = true;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                for (int t = 0; t < 2; ++t) {
-                    if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(kv_full(stage), L::kTileBytes);
-                    const void *tm = t ? static_cast<const void *>(&tmV) : static_cast<const void *>(&tmK);
-#pragma unroll
-                    for (int a = 0; a < L::kAtoms; ++a)
-                        tma_load_3d(sKV + stage * L::kTileBytes + a * L::kAtomBytes, tm, a * 64,
-                                    j * kBN, kvh, kv_full(stage));
-                    used |= 1u << stage;
-                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+    if (warp >= 2 && warp < 4) {
+        // ---------------------------------------------------- loaders (warps 2, 3)
+        const int ltid = threadIdx.x - 64;
+        const size_t head_bytes = static_cast<size_t>(p.N) * D * 2;
+        const uint8_t *kh = p.k + static_cast<size_t>(kvh) * head_bytes;
+        const uint8_t *vh = p.v + static_cast<size_t>(kvh) * head_bytes;
+        LoadSignal sig;
+        if (!p.inject_stall) {
+            load_tile<D>(sQ, p.q + static_cast<size_t>(bh) * head_bytes, q0, p.N, ltid);
+            sig.commit(q_full);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int j = 0; j < n_kv && ok; ++j) {
+            for (int t = 0; t < 2; ++t) {
+                if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                load_tile<D>(sKV + stage * L::kTileBytes, t ? vh : kh, j * kBN, p.N, ltid);
+                sig.commit(kv_full(stage));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            // Every copy issued must have landed before the CTA may exit.
-            if (issued_q) drain_bar(q_full, 0, p);
-            for (int s = 0; s < kStages; ++s)
-                if (used >> s & 1u) drain_bar(kv_full(s), last_phase >> s & 1u, p);
         }
+        // Announce the last group; every copy has landed before the CTA exits.
+        sig.announce<true>();
+        cp_async_wait<0>();
     } else if (warp == 1) {
         if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+            // ---------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, kBM, kBN, false);
             constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, kBM, D, true);
             const uint32_t tS = tmem, tO = tmem + kTmemO;
@@ -181,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sK = sKV + stage * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
                     mma_f16_ss(tS, sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(sK + koff, 16, 1024),
                                idesc_qk, kk > 0);
                 }
@@ -200,9 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sV = sKV + stage * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint32_t poff = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+                    const uint32_t poff = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
                     mma_f16_ss(tO, sdesc_sw128(sP + poff, 16, 1024),
-                               sdesc_sw128(sV + kk * 2048, L::kAtomBytes, 1024), idesc_pv,
+                               sdesc_sw128(sV + kk * 2048, kAtomBytes, 1024), idesc_pv,
                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(o_full);
@@ -289,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     e[t] = ex2_approx(fmaf(u2f(s[ch * 8 + t]), c, -mc));
                     l += e[t];
                 }
-                const uint32_t addr = prow + (ch >> 3) * L::kAtomBytes + (((ch & 7) ^ (r & 7)) << 4);
+                const uint32_t addr = prow + (ch >> 3) * kAtomBytes + (((ch & 7) ^ (r & 7)) << 4);
                 st_shared_v4(addr, pack2<kBF16>(e[0], e[1]), pack2<kBF16>(e[2], e[3]),
                              pack2<kBF16>(e[4], e[5]), pack2<kBF16>(e[6], e[7]));
             }
@@ -347,37 +334,6 @@ void note_cuda_error(cudaError_t e, const char *where) {
     std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", where, cudaGetErrorString(e));
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// [rows = BH * N, D] viewed as 3-D (D, N, BH) so that a box never crosses
-// from one head into the next: rows past N read as zeros.
-bool encode_qkv_map(CUtensorMap *map, const void *base, bool bf16, int D, int N, long long BH) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 int g_dev_state[kMaxDevices];      // 0 unknown, 1 sm_103, -1 other
@@ -411,8 +367,7 @@ attn_status_t check_device(int *dev_out) {
 }
 
 template <int D, bool BF16, bool CAUSAL>
-attn_status_t launch(int dev, int kid, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                     gqa::Params prm, cudaStream_t stream) {
+attn_status_t launch(int dev, int kid, const gqa::Params &prm, cudaStream_t stream) {
     const bool persistent = g_kernel_choice.load() == 0;
     auto kern = persistent ? gqa::attn_fwd_ws_kernel<D, BF16, CAUSAL> : gqa::attn_fwd_kernel<D, BF16, CAUSAL>;
     const int smem = persistent ? gqa::WsLayout<D>::kAlloc : gqa::Layout<D>::kAlloc;
@@ -436,7 +391,7 @@ attn_status_t launch(int dev, int kid, const CUtensorMap &tq, const CUtensorMap 
             g_dev_smem_set[dev] |= 1u << kid;
         }
     }
-    kern<<<grid, threads, smem, stream>>>(tq, tk, tv, prm);
+    kern<<<grid, threads, smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         note_cuda_error(e, "kernel launch");
@@ -462,7 +417,6 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
         (lse && misaligned(lse, 4)))
         return ATTN_ERR_ALIGN;
     const long long BHq = static_cast<long long>(B) * Hq;
-    const long long BHkv = static_cast<long long>(B) * Hkv;
     const int n_tiles = (N + gqa::kBN - 1) / gqa::kBN;
     if (BHq * n_tiles > INT_MAX) return ATTN_ERR_SHAPE;
 
@@ -471,13 +425,10 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
     if (st != ATTN_OK) return st;
 
     const bool bf16 = dtype == ATTN_BF16;
-    CUtensorMap tq, tk, tv;
-    if (!encode_qkv_map(&tq, q, bf16, D, N, BHq) || !encode_qkv_map(&tk, k, bf16, D, N, BHkv) ||
-        !encode_qkv_map(&tv, v, bf16, D, N, BHkv)) {
-        std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
-        return ATTN_ERR_LAUNCH;
-    }
     gqa::Params prm;
+    prm.q = static_cast<const uint8_t *>(q);
+    prm.k = static_cast<const uint8_t *>(k);
+    prm.v = static_cast<const uint8_t *>(v);
     prm.o = o;
     prm.lse = lse;
     prm.N = N;
@@ -494,14 +445,14 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (kid) {
-        case 0: return launch<64, false, false>(dev, kid, tq, tk, tv, prm, s);
-        case 1: return launch<64, false, true>(dev, kid, tq, tk, tv, prm, s);
-        case 2: return launch<64, true, false>(dev, kid, tq, tk, tv, prm, s);
-        case 3: return launch<64, true, true>(dev, kid, tq, tk, tv, prm, s);
-        case 4: return launch<128, false, false>(dev, kid, tq, tk, tv, prm, s);
-        case 5: return launch<128, false, true>(dev, kid, tq, tk, tv, prm, s);
-        case 6: return launch<128, true, false>(dev, kid, tq, tk, tv, prm, s);
-        default: return launch<128, true, true>(dev, kid, tq, tk, tv, prm, s);
+        case 0: return launch<64, false, false>(dev, kid, prm, s);
+        case 1: return launch<64, false, true>(dev, kid, prm, s);
+        case 2: return launch<64, true, false>(dev, kid, prm, s);
+        case 3: return launch<64, true, true>(dev, kid, prm, s);
+        case 4: return launch<128, false, false>(dev, kid, prm, s);
+        case 5: return launch<128, false, true>(dev, kid, prm, s);
+        case 6: return launch<128, true, false>(dev, kid, prm, s);
+        default: return launch<128, true, true>(dev, kid, prm, s);
     }
 }
 

@@ -6,9 +6,11 @@
 // (deepseek.csdn.net/6a3201f8..., sections "在线softmax" and "FlashAttention").
 //
 // Roles (384 threads):
-//   warp 0        TMA producer: Q0, K_0, Q1, V_0, K_1, V_1, ... into a ring of
-//                 kStagesWs 128-byte-swizzled tiles (full / empty mbarriers).
-//   warp 1        MMA issuer (one lane):  S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per
+//   warps 2-3     loaders: K_0, (Q0, Q1), V_0, K_1, V_1, ... with 16-byte cp.async
+//                 into a ring of kStagesWs 128-byte-swizzled tiles (full / empty
+//                 mbarriers); each group of copies is announced one group late.
+//   warp 1        allocates and frees the 512 TMEM columns.
+//   warp 0        MMA issuer (one lane):  S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per
 //                 key tile j:  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,
 //                 S1 = Q1 K_{j+1}^T.  While softmax warpgroup 0 works on S0 the
 //                 tensor core runs tile 1's products, and the other way round.
@@ -36,20 +38,23 @@ namespace gqa {
 constexpr int kWsThreads = 384;
 constexpr int kStagesWs = 4;
 constexpr uint32_t kWsTmemCols = 512;
-constexpr uint32_t kRegsLow = 88;   // warps 0-3 after the hand-off
-constexpr uint32_t kRegsHigh = 208;  // softmax warpgroups after the hand-off (128*88 + 256*208 = 384*168)
+// A tile's probabilities are split into two input-type terms (P_hi + P_lo)
+// when some row's running sum, in units of its largest weight, is below this.
+constexpr float kSplitL = 16.f;
+constexpr uint32_t kRegsLow = 112;   // warps 0-3 after the hand-off
+constexpr uint32_t kRegsHigh = 192;  // softmax warpgroups after the hand-off (128*112 + 256*192 <= 384*168)
 
 template <int D>
 struct WsLayout {
     static constexpr int kAtoms = D / 64;
-    static constexpr int kAtomBytes = 128 * 128;  // 128 rows x 128 B
     static constexpr int kTileBytes = kAtoms * kAtomBytes;
     static constexpr int kQ = 0;  // Q0, Q1
     static constexpr int kKV = kQ + 2 * kTileBytes;
     static constexpr int kBar = kKV + kStagesWs * kTileBytes;
     // q_full[2], q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], mma_done
     static constexpr int kNumBars = 2 + 1 + 2 * kStagesWs + 2 + 2 + 2 + 1;
-    static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kFlags = kBar + kNumBars * 8;  // split flags [2 tiles][4 warps]
+    static constexpr int kTmemSlot = kFlags + 32;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kUsed = kAbort + 4;
     // at least half of the SM's shared memory, so that one CTA (which takes all
@@ -90,8 +95,7 @@ __device__ __forceinline__ int ws_tiles(const Params &p, int qb, int i) {
 
 template <int D, bool kBF16, bool kCausal>
 __global__ void __launch_bounds__(kWsThreads, 1)
-    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const Params p) {
+    attn_fwd_ws_kernel(const Params p) {
     using L = WsLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -109,15 +113,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t mma_done = bar0 + 8u * (9 + 2 * kStagesWs);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
+    volatile uint32_t *flags = reinterpret_cast<volatile uint32_t *>(smem + L::kFlags);
+    auto split_flag = [&](int i, int w) -> volatile uint32_t & { return flags[4 * i + w]; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
-        mbar_init(q_full(0), 1);
-        mbar_init(q_full(1), 1);
+        mbar_init(q_full(0), kLoaderThreads);
+        mbar_init(q_full(1), kLoaderThreads);
         mbar_init(q_empty, 1);
         for (int s = 0; s < kStagesWs; ++s) {
-            mbar_init(kv_full(s), 1);
+            mbar_init(kv_full(s), kLoaderThreads);
             mbar_init(kv_empty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -141,62 +147,48 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     if (warp < 4) {
         regs_dec<kRegsLow>();
-        if (warp == 0 && lane == 0) {
-            // ---------------------------------------------------- TMA producer
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
+        if (warp >= 2) {
+            // ---------------------------------------------------- loaders (warps 2, 3)
+            const int ltid = threadIdx.x - 64;
             Ring ring;
-            uint32_t used = 0, last_phase = 0;
+            LoadSignal sig;
             int items = 0;
             bool ok = true;
-            auto load_kv = [&](const void *tm, int row, int kvh) -> bool {
+            auto load_kv = [&](const uint8_t *head, int row0) -> bool {
                 if (!wait_bar(kv_empty(ring.s), ring.ph ^ 1u, p, abort_flag)) return false;
-                mbar_arrive_expect_tx(kv_full(ring.s), L::kTileBytes);
-#pragma unroll
-                for (int a = 0; a < L::kAtoms; ++a)
-                    tma_load_3d(sKV + ring.s * L::kTileBytes + a * L::kAtomBytes, tm, a * 64, row, kvh,
-                                kv_full(ring.s));
-                used |= 1u << ring.s;
-                last_phase = (last_phase & ~(1u << ring.s)) | (ring.ph << ring.s);
+                load_tile<D>(sKV + ring.s * L::kTileBytes, head, row0, p.N, ltid);
+                sig.commit(kv_full(ring.s));
                 ring.next();
                 return true;
             };
             for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
                 int bh, qb;
                 if (!ws_item(p, r, bh, qb)) continue;
-                const int kvh = bh / p.group;
+                const size_t head_bytes = static_cast<size_t>(p.N) * D * 2;
+                const uint8_t *qh = p.q + static_cast<size_t>(bh) * head_bytes;
+                const uint8_t *kh = p.k + static_cast<size_t>(bh / p.group) * head_bytes;
+                const uint8_t *vh = p.v + static_cast<size_t>(bh / p.group) * head_bytes;
                 const int q0 = qb * 256;
                 const int n1 = ws_tiles<kCausal>(p, qb, 1);
                 // K_0 may land while the previous item still runs; the Q buffers
                 // are free once every S MMA of the previous item is done.
-                if (!load_kv(&tmK, 0, kvh)) break;
-                if (!wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag)) break;
+                if (!(ok = load_kv(kh, 0))) break;
+                if (!(ok = wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag))) break;
                 if (!p.inject_stall) {
-                    mbar_arrive_expect_tx(q_full(0), L::kTileBytes);
-#pragma unroll
-                    for (int a = 0; a < L::kAtoms; ++a)
-                        tma_load_3d(sQ + a * L::kAtomBytes, &tmQ, a * 64, q0, bh, q_full(0));
-                    mbar_arrive_expect_tx(q_full(1), L::kTileBytes);
-#pragma unroll
-                    for (int a = 0; a < L::kAtoms; ++a)
-                        tma_load_3d(sQ + L::kTileBytes + a * L::kAtomBytes, &tmQ, a * 64, q0 + 128, bh,
-                                    q_full(1));
+                    load_tile<D>(sQ, qh, q0, p.N, ltid);
+                    load_tile<D>(sQ + L::kTileBytes, qh, q0 + 128, p.N, ltid);
+                    sig.commit(q_full(0), q_full(1));
                 }
                 ++items;
                 for (int j = 0; j < n1 && ok; ++j) {
-                    ok = load_kv(&tmV, j * kBN, kvh);
-                    if (ok && j + 1 < n1) ok = load_kv(&tmK, (j + 1) * kBN, kvh);
+                    ok = load_kv(vh, j * kBN);
+                    if (ok && j + 1 < n1) ok = load_kv(kh, (j + 1) * kBN);
                 }
             }
-            // Every copy issued must have landed before the CTA may exit.
-            if (items > 0 && !p.inject_stall) {
-                drain_bar(q_full(0), (items - 1) & 1, p);
-                drain_bar(q_full(1), (items - 1) & 1, p);
-            }
-            for (int s = 0; s < kStagesWs; ++s)
-                if (used >> s & 1u) drain_bar(kv_full(s), last_phase >> s & 1u, p);
-        } else if (warp == 1 && lane == 0) {
+            // Announce the last group; every copy has landed before the CTA exits.
+            sig.announce<true>();
+            cp_async_wait<0>();
+        } else if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, 128, kBN, false);
             constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, 128, D, true);
@@ -208,18 +200,27 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const uint32_t a0 = sQ + i * L::kTileBytes, b0 = sKV + kstage * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+                    const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
                     mma_f16_ss(tmem + 128u * i, sdesc_sw128(a0 + off, 16, 1024),
                                sdesc_sw128(b0 + off, 16, 1024), idesc_qk, kk > 0);
                 }
             };
+            // O_i (+)= P_i V: P_hi from the first 64 columns of S_i, and, when the
+            // softmax warpgroup split this tile, P_lo from the next 64.
             auto pv = [&](int i, int vstage, bool acc) {
                 const uint32_t b0 = sKV + vstage * L::kTileBytes;
+                const bool split = (split_flag(i, 0) | split_flag(i, 1) | split_flag(i, 2) | split_flag(i, 3)) != 0;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     mma_f16_ts(tmem + 256u + 128u * i, tmem + 128u * i + 8u * kk,
-                               sdesc_sw128(b0 + kk * 2048, L::kAtomBytes, 1024), idesc_pv,
+                               sdesc_sw128(b0 + kk * 2048, kAtomBytes, 1024), idesc_pv,
                                (acc || kk > 0) ? 1u : 0u);
+                if (split) {
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_f16_ts(tmem + 256u + 128u * i, tmem + 128u * i + 64u + 8u * kk,
+                                   sdesc_sw128(b0 + kk * 2048, kAtomBytes, 1024), idesc_pv, 1u);
+                }
             };
             for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
                 int bh, qb;
@@ -334,7 +335,40 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 const float m_new = fmaxf(m, mt);
                 const float alpha = ex2_approx((m - m_new) * c);  // 0 on the first tile
-                if (j > 0 && __any_sync(0xffffffffu, m_new > m)) {
+                const bool grew = m_new > m;
+                m = m_new;
+                const float mc = m * c;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int cc = 0; cc < 128; ++cc) {
+                    const float e = ex2_approx(fmaf(u2f(s[cc]), c, -mc));
+                    ls[cc & 3] += e;
+                    s[cc] = __float_as_uint(e);
+                }
+                l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                // Split P = P_hi + P_lo for the whole tile when any row of the
+                // warpgroup still has its weight on few keys (running sum < kSplitL
+                // in units of its largest weight); decided jointly by the 4 warps.
+                const uint32_t need = __any_sync(0xffffffffu, l < kSplitL) ? 1u : 0u;
+                if (lane == 0) split_flag(i, wq) = need;
+                named_bar_sync(1 + i, 128);
+                const bool split = (split_flag(i, 0) | split_flag(i, 1) | split_flag(i, 2) | split_flag(i, 3)) != 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) pk[t] = pack2<kBF16>(u2f(s[32 * q + 2 * t]), u2f(s[32 * q + 2 * t + 1]));
+                    tmem_st16(tS + 16 * q, pk);
+                    if (split) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float2 h = unpack2<kBF16>(pk[t]);
+                            pk[t] = pack2<kBF16>(u2f(s[32 * q + 2 * t]) - h.x, u2f(s[32 * q + 2 * t + 1]) - h.y);
+                        }
+                        tmem_st16(tS + 64 + 16 * q, pk);
+                    }
+                }
+                if (j > 0 && __any_sync(0xffffffffu, grew)) {
                     // O_i holds P_i V_{j-1} already (covered by the S_i(j) commit).
                     __syncwarp();
 #pragma unroll
@@ -347,23 +381,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         tmem_st32(tO + 32 * q, o);
                     }
                 }
-                m = m_new;
-                const float mc = m * c;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const float e0 = ex2_approx(fmaf(u2f(s[64 * q + 2 * t]), c, -mc));
-                        const float e1 = ex2_approx(fmaf(u2f(s[64 * q + 2 * t + 1]), c, -mc));
-                        ls[(2 * t) & 3] += e0;
-                        ls[(2 * t + 1) & 3] += e1;
-                        pk[t] = pack2<kBF16>(e0, e1);
-                    }
-                    tmem_st32(tS + 32 * q, pk);
-                }
-                l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(p_full(i));

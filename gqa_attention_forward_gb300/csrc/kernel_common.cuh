@@ -1,5 +1,6 @@
 // Pieces shared by the attention kernels: launch parameters, the device
-// error word, bounded mbarrier waits and small conversions.
+// error word, bounded mbarrier waits, the cp.async tile loader and small
+// conversions.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -20,6 +21,9 @@ __device__ int g_error_code;
 __device__ unsigned int g_abort_seq;
 
 struct Params {
+    const uint8_t *q;  // [B*Hq, N, D] elements of 2 bytes
+    const uint8_t *k;  // [B*Hkv, N, D]
+    const uint8_t *v;  // [B*Hkv, N, D]
     void *o;
     float *lse;
     int N;
@@ -71,6 +75,58 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, const P
     }
 }
 
+constexpr int kLoaderThreads = 64;  // warps 2 and 3 of either kernel
+constexpr int kAtomBytes = 128 * 128;  // 128 rows x 128 B: one 128-byte swizzle atom column
+
+// Copies rows [row0, row0 + 128) of one head ([N, D], 2-byte elements, D
+// fastest) into a shared-memory tile in the UMMA K-major 128-byte-swizzle
+// layout: columns [64a, 64a + 64) of row r sit in atom a at r * 128 bytes, and
+// 16-byte chunk c of that 128-byte row is stored at chunk c ^ (r % 8).  Rows
+// at or past N are zero-filled.  Each of the 64 loader threads owns one
+// 16-byte column chunk and every (64 / chunks-per-row)-th row, so a warp
+// reads 512 contiguous bytes per instruction.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const uint8_t *head, int row0, int N, int ltid) {
+    constexpr int kChunksPerRow = D / 8;
+    constexpr int kRowStep = kLoaderThreads / kChunksPerRow;
+    const int cc = ltid % kChunksPerRow;
+    const int r0 = ltid / kChunksPerRow;
+    const uint32_t col = (cc >> 3) * kAtomBytes;
+    const uint8_t *src_col = head + cc * 16;
+#pragma unroll 8
+    for (int i = 0; i < 128 / kRowStep; ++i) {
+        const int r = r0 + i * kRowStep;
+        const int row = row0 + r;
+        const bool in = row < N;
+        const uint8_t *src = src_col + static_cast<size_t>(in ? row : 0) * (D * 2);
+        cp_async_16(dst + col + r * 128 + (((cc & 7) ^ (r & 7)) << 4), src, in ? 16u : 0u);
+    }
+}
+
+// Completion protocol of the loader threads: each committed cp.async group is
+// announced one group late (wait for all but the newest group, make the data
+// visible to the tensor core's async proxy, then arrive on its barriers), so
+// that copies of consecutive tiles overlap.
+struct LoadSignal {
+    uint32_t bar_a = 0, bar_b = 0;  // barriers of the newest, not yet announced group
+    template <bool kAll>
+    __device__ __forceinline__ void announce() {
+        if (bar_a == 0) return;
+        if (kAll) cp_async_wait<0>(); else cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(bar_a);
+        if (bar_b != 0) mbar_arrive(bar_b);
+        bar_a = bar_b = 0;
+    }
+    // Commit the group just issued; announce the one before it.
+    __device__ __forceinline__ void commit(uint32_t a, uint32_t b = 0) {
+        cp_async_commit();
+        announce<false>();
+        bar_a = a;
+        bar_b = b;
+    }
+};
+
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (kBF16) {
@@ -79,6 +135,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     } else {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+// The two halves of a packed pair as floats (exact).
+template <bool kBF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (kBF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    } else {
+        __half2 h = *reinterpret_cast<__half2 *>(&w);
+        return __half22float2(h);
     }
 }
 

@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the sm_103a features the attention kernel uses:
-// mbarriers, TMA tensor loads, tcgen05 (TMEM allocation, MMA, commit, TMEM
+// mbarriers, cp.async copies, tcgen05 (TMEM allocation, MMA, commit, TMEM
 // loads/stores, fences) and the fast base-2 exponential.  Encodings of the
 // UMMA shared-memory and instruction descriptors follow the PTX ISA
 // description of tcgen05 matrix descriptors.
@@ -44,19 +44,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// ---------------------------------------------------------------- TMA
-__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+// ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy that bypasses L1; src_bytes < 16 zero-fills
+// the rest of the 16 bytes (0 reads nothing).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
 }
-// 3-D tiled load of one box into shared memory; completion is signalled on
-// `bar` as transaction bytes.  c0 is the innermost (element) coordinate.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
-                                            int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -158,6 +159,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
 // Wait for this thread's TMEM loads; the empty asm statements then tie each
 // loaded register to the wait so no use of it is scheduled before the wait.
 template <int K>
@@ -178,6 +188,11 @@ __device__ __forceinline__ void regs_dec() {
 template <uint32_t R>
 __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- math
