@@ -287,7 +287,7 @@ def run_ours(args):
                          "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": None,
                          "peak_source": f"{peak_src} "
                                         f"{'sustained' if long_region else 'burst'} bf16",
-                         "kernel": "gqa::attn_fwd_kernel", "kernel_ms": round(kern_ms, 4),
+                         "kernel": "gqa::attn_fwd_ws_kernel", "kernel_ms": round(kern_ms, 4),
                          "frac_of_2250_nominal": round(achieved / 2250.0, 4)},
             "e2e": {"value": round(world * w.flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -41,6 +41,9 @@ constexpr uint32_t kWsTmemCols = 512;
 // A tile's probabilities are split into two input-type terms (P_hi + P_lo)
 // when some row's running sum, in units of its largest weight, is below this.
 constexpr float kSplitL = 16.f;
+// The probabilities are referenced to a stale row max until the true max
+// exceeds it by more than this many powers of two (P <= 2^8 meanwhile).
+constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kRegsLow = 112;   // warps 0-3 after the hand-off
 constexpr uint32_t kRegsHigh = 192;  // softmax warpgroups after the hand-off (128*112 + 256*192 <= 384*168)
 
@@ -196,31 +199,34 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             uint32_t pcount[2] = {0, 0};
             int items = 0;
             bool ok = true;
+            // Descriptors are built once per operand tile; stepping K by 16 moves
+            // the start address by 32 B within a swizzle atom (+2 in the 16-byte
+            // address field) and by one 16 KB atom every 4 steps (+1024).
+            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dkv0 = sdesc_sw128(sKV, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sKV, kAtomBytes, 1024);
             auto qk = [&](int i, int kstage) {
-                const uint32_t a0 = sQ + i * L::kTileBytes, b0 = sKV + kstage * L::kTileBytes;
+                uint64_t a = dq0 + static_cast<uint64_t>(i * (L::kTileBytes >> 4));
+                uint64_t b = dkv0 + static_cast<uint64_t>(kstage * (L::kTileBytes >> 4));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-                    mma_f16_ss(tmem + 128u * i, sdesc_sw128(a0 + off, 16, 1024),
-                               sdesc_sw128(b0 + off, 16, 1024), idesc_qk, kk > 0);
+                    const uint64_t off = (kk >> 2) * (kAtomBytes >> 4) + (kk & 3) * 2;
+                    mma_f16_ss(tmem + 128u * i, a + off, b + off, idesc_qk, kk > 0);
                 }
             };
-            // O_i (+)= P_i V: P_hi from the first 64 columns of S_i, and, when the
-            // softmax warpgroup split this tile, P_lo from the next 64.
+            // O_i (+)= P_i V: P_hi from the first 64 columns of S_i, and, when a
+            // softmax warp split this tile, P_lo from the next 64.
             auto pv = [&](int i, int vstage, bool acc) {
-                const uint32_t b0 = sKV + vstage * L::kTileBytes;
+                const uint64_t b0 = dv0 + static_cast<uint64_t>(vstage * (L::kTileBytes >> 4));
+                const uint32_t ta = tmem + 128u * i, td = tmem + 256u + 128u * i;
                 const bool split = (split_flag(i, 0) | split_flag(i, 1) | split_flag(i, 2) | split_flag(i, 3)) != 0;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_f16_ts(tmem + 256u + 128u * i, tmem + 128u * i + 8u * kk,
-                               sdesc_sw128(b0 + kk * 2048, kAtomBytes, 1024), idesc_pv,
-                               (acc || kk > 0) ? 1u : 0u);
-                if (split) {
+                const int passes = split ? 2 : 1;
+#pragma unroll 1
+                for (int h = 0; h < passes; ++h)
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_f16_ts(tmem + 256u + 128u * i, tmem + 128u * i + 64u + 8u * kk,
-                                   sdesc_sw128(b0 + kk * 2048, kAtomBytes, 1024), idesc_pv, 1u);
-                }
+                        mma_f16_ts(td, ta + 64u * h + 8u * kk, b0 + kk * (2048 >> 4), idesc_pv,
+                                   (acc || kk > 0 || h > 0) ? 1u : 0u);
             };
             for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
                 int bh, qb;
@@ -300,7 +306,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const int n = ws_tiles<kCausal>(p, qb, i);
             const int row0 = qb * 256 + 128 * i;  // first query row of this tile
             const int diag = row0 / kBN;           // causal: the one masked key tile
-            float m = -INFINITY, l = 0.f;
+            // m_ref: the max the probabilities are taken against (updated lazily);
+            // m_top: the true running row max; l: running sum in units of 2^(m_ref*c).
+            float m_ref = -INFINITY, m_top = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 if (!__all_sync(0xffffffffu, wait_bar(s_full(i), scount & 1u, p, abort_flag))) {
                     ok = false;
@@ -326,31 +334,44 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     for (int cc = 0; cc < 128; ++cc)
                         if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
                 }
-                float mx[8];
+                float mx[4] = {u2f(s[0]), u2f(s[1]), u2f(s[2]), u2f(s[3])};
 #pragma unroll
-                for (int t = 0; t < 8; ++t) mx[t] = u2f(s[t]);
+                for (int cc = 4; cc < 128; cc += 8)
 #pragma unroll
-                for (int cc = 8; cc < 128; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], u2f(s[cc]));
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                const float m_new = fmaxf(m, mt);
-                const float alpha = ex2_approx((m - m_new) * c);  // 0 on the first tile
-                const bool grew = m_new > m;
-                m = m_new;
-                const float mc = m * c;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int cc = 0; cc < 128; ++cc) {
-                    const float e = ex2_approx(fmaf(u2f(s[cc]), c, -mc));
-                    ls[cc & 3] += e;
-                    s[cc] = __float_as_uint(e);
+                    for (int k = 0; k < 4; ++k) mx[k] = fmax3(mx[k], u2f(s[cc + 2 * k]), u2f(s[cc + 2 * k + 1]));
+                m_top = fmaxf(m_top, fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])));
+                // Re-reference only when the max has grown by more than kRescaleLog2
+                // (in log2 units) since the last reference; otherwise P may exceed 1.
+                float alpha = 1.f;
+                bool rescale = false;
+                if (m_ref == -INFINITY) {
+                    m_ref = m_top;  // first tile: the accumulator is still empty
+                } else if ((m_top - m_ref) * c > kRescaleLog2) {
+                    alpha = ex2_approx((m_ref - m_top) * c);
+                    m_ref = m_top;
+                    rescale = true;
                 }
-                l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-                // Split P = P_hi + P_lo for the whole tile when any row of the
-                // warpgroup still has its weight on few keys (running sum < kSplitL
-                // in units of its largest weight); decided jointly by the 4 warps.
-                const uint32_t need = __any_sync(0xffffffffu, l < kSplitL) ? 1u : 0u;
-                if (lane == 0) split_flag(i, wq) = need;
+                const float2 c2 = make_float2(c, c);
+                const float2 nmc2 = make_float2(-m_ref * c, -m_ref * c);
+                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int cc = 0; cc < 128; cc += 2) {
+                    float2 e = ffma2(make_float2(u2f(s[cc]), u2f(s[cc + 1])), c2, nmc2);
+                    e.x = ex2_approx(e.x);
+                    e.y = ex2_approx(e.y);
+                    acc[(cc >> 1) & 1] = fadd2(acc[(cc >> 1) & 1], e);
+                    s[cc] = __float_as_uint(e.x);
+                    s[cc + 1] = __float_as_uint(e.y);
+                }
+                const float2 sum2 = fadd2(acc[0], acc[1]);
+                l = l * alpha + (sum2.x + sum2.y);
+                // Split P = P_hi + P_lo for the whole tile when some row of the
+                // warpgroup has its weight on few keys: its running sum relative to
+                // its largest weight 2^((m_top - m_ref) c) is below kSplitL.  The
+                // four warps agree through a named barrier.
+                const bool need = l * ex2_approx((m_ref - m_top) * c) < kSplitL;
+                if (lane == 0) split_flag(i, wq) = __any_sync(0xffffffffu, need) ? 1u : 0u;
+                else __any_sync(0xffffffffu, need);
                 named_bar_sync(1 + i, 128);
                 const bool split = (split_flag(i, 0) | split_flag(i, 1) | split_flag(i, 2) | split_flag(i, 3)) != 0;
 #pragma unroll
@@ -368,7 +389,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         tmem_st16(tS + 64 + 16 * q, pk);
                     }
                 }
-                if (j > 0 && __any_sync(0xffffffffu, grew)) {
+                if (__any_sync(0xffffffffu, rescale)) {
                     // O_i holds P_i V_{j-1} already (covered by the S_i(j) commit).
                     __syncwarp();
 #pragma unroll
@@ -395,7 +416,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             tc_fence_after();
             __syncwarp();
             const int row = row0 + r;
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / l;  // l is in units of 2^(m_ref * c)
             uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.N + row) * (D * 2);
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
@@ -414,7 +435,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
             }
             if (p.lse != nullptr && row < p.N)
-                p.lse[static_cast<size_t>(bh) * p.N + row] = (m * c + log2f(l)) * 0.6931471805599453f;
+                p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref * c + log2f(l)) * 0.6931471805599453f;
             // O_i is read; the next item's first P_i V MMA waits for this warpgroup's p_full.
             tc_fence_before();
         }

@@ -93,7 +93,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const uint8_t *head, int
     const int r0 = ltid / kChunksPerRow;
     const uint32_t col = (cc >> 3) * kAtomBytes;
     const uint8_t *src_col = head + cc * 16;
-#pragma unroll 8
+#pragma unroll 4
     for (int i = 0; i < 128 / kRowStep; ++i) {
         const int r = r0 + i * kRowStep;
         const int row = row0 + r;
