@@ -8,7 +8,8 @@
 // Roles (384 threads):
 //   warps 2-3     loaders: K_0, (Q0, Q1), V_0, K_1, V_1, ... with 16-byte cp.async
 //                 into a ring of kStagesWs 128-byte-swizzled tiles (full / empty
-//                 mbarriers); each group of copies is announced one group late.
+//                 mbarriers); each thread's copies arrive on the full barrier
+//                 when they land (cp.async.mbarrier.arrive).
 //   warp 1        allocates and frees the 512 TMEM columns.
 //   warp 0        MMA issuer (one lane):  S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per
 //                 key tile j:  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,
@@ -154,13 +155,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             // ---------------------------------------------------- loaders (warps 2, 3)
             const int ltid = threadIdx.x - 64;
             Ring ring;
-            LoadSignal sig;
             int items = 0;
             bool ok = true;
+            // Each loader thread's copies of a tile arrive on the tile's barrier as
+            // soon as they land (64 arrivals complete it).
             auto load_kv = [&](const uint8_t *head, int row0) -> bool {
                 if (!wait_bar(kv_empty(ring.s), ring.ph ^ 1u, p, abort_flag)) return false;
                 load_tile<D>(sKV + ring.s * L::kTileBytes, head, row0, p.N, ltid);
-                sig.commit(kv_full(ring.s));
+                cp_async_arrive(kv_full(ring.s));
                 ring.next();
                 return true;
             };
@@ -179,8 +181,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 if (!(ok = wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag))) break;
                 if (!p.inject_stall) {
                     load_tile<D>(sQ, qh, q0, p.N, ltid);
+                    cp_async_arrive(q_full(0));
                     load_tile<D>(sQ + L::kTileBytes, qh, q0 + 128, p.N, ltid);
-                    sig.commit(q_full(0), q_full(1));
+                    cp_async_arrive(q_full(1));
                 }
                 ++items;
                 for (int j = 0; j < n1 && ok; ++j) {
@@ -188,8 +191,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     if (ok && j + 1 < n1) ok = load_kv(kh, (j + 1) * kBN);
                 }
             }
-            // Announce the last group; every copy has landed before the CTA exits.
-            sig.announce<true>();
+            // Every copy has landed before the CTA exits.
+            cp_async_commit();
             cp_async_wait<0>();
         } else if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- MMA issuer
@@ -235,10 +238,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const uint32_t ip = items & 1;
                 if (!(ok = wait_bar(q_full(0), ip, p, abort_flag))) break;
                 if (!(ok = wait_bar(kv_full(ring.s), ring.ph, p, abort_flag))) break;
+                fence_proxy_async_smem();  // cp.async data -> tensor core reads
                 tc_fence_after();
                 qk(0, ring.s);
                 mma_commit(s_full(0));
                 if (!(ok = wait_bar(q_full(1), ip, p, abort_flag))) break;
+                fence_proxy_async_smem();
                 tc_fence_after();
                 qk(1, ring.s);
                 mma_commit(s_full(1));
@@ -247,6 +252,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 for (int j = 0; j < n1; ++j) {
                     const int vs = ring.s;
                     if (!(ok = wait_bar(kv_full(vs), ring.ph, p, abort_flag))) break;
+                    fence_proxy_async_smem();
                     ring.next();
                     if (j < n0) {
                         if (!(ok = wait_bar(p_full(0), pcount[0] & 1u, p, abort_flag))) break;
@@ -259,6 +265,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const int ks = ring.s;
                     if (more) {
                         if (!(ok = wait_bar(kv_full(ks), ring.ph, p, abort_flag))) break;
+                        fence_proxy_async_smem();
                         tc_fence_after();
                         if (j + 1 < n0) {
                             qk(0, ks);
@@ -334,12 +341,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     for (int cc = 0; cc < 128; ++cc)
                         if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
                 }
-                float mx[4] = {u2f(s[0]), u2f(s[1]), u2f(s[2]), u2f(s[3])};
+                float mx[8];  // eight independent chains of 3-input max
 #pragma unroll
-                for (int cc = 4; cc < 128; cc += 8)
+                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(u2f(s[2 * k]), u2f(s[2 * k + 1]));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) mx[k] = fmax3(mx[k], u2f(s[cc + 2 * k]), u2f(s[cc + 2 * k + 1]));
-                m_top = fmaxf(m_top, fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])));
+                for (int cc = 16; cc < 128; cc += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], u2f(s[cc + 2 * k]), u2f(s[cc + 2 * k + 1]));
+                m_top = fmaxf(m_top, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 // Re-reference only when the max has grown by more than kRescaleLog2
                 // (in log2 units) since the last reference; otherwise P may exceed 1.
                 float alpha = 1.f;

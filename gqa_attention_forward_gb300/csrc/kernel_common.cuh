@@ -88,18 +88,29 @@ constexpr int kAtomBytes = 128 * 128;  // 128 rows x 128 B: one 128-byte swizzle
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const uint8_t *head, int row0, int N, int ltid) {
     constexpr int kChunksPerRow = D / 8;
-    constexpr int kRowStep = kLoaderThreads / kChunksPerRow;
+    constexpr int kRowStep = kLoaderThreads / kChunksPerRow;  // rows between a thread's copies
+    constexpr int kIters = 128 / kRowStep;
     const int cc = ltid % kChunksPerRow;
-    const int r0 = ltid / kChunksPerRow;
+    const int r0 = ltid / kChunksPerRow;  // < kRowStep <= 8
     const uint32_t col = (cc >> 3) * kAtomBytes;
-    const uint8_t *src_col = head + cc * 16;
+    // Row r0 + i*kRowStep has swizzle phase (r0 + i*kRowStep) % 8: constant when the
+    // step is 8, alternating between two values when it is 4.
+    const uint32_t d_even = dst + col + r0 * 128 + (((cc & 7) ^ (r0 & 7)) << 4);
+    const uint32_t d_odd = dst + col + r0 * 128 + (((cc & 7) ^ ((r0 + kRowStep) & 7)) << 4);
+    const uint8_t *src = head + static_cast<size_t>(row0 + r0) * (D * 2) + cc * 16;
+    if (row0 + 128 <= N) {
+        // whole tile in range: every copy is a base plus a compile-time offset
+#pragma unroll
+        for (int i = 0; i < kIters; ++i)
+            cp_async_16(((i & 1) ? d_odd : d_even) + i * kRowStep * 128, src + i * kRowStep * (D * 2), 16u);
+    } else {
+        const uint8_t *row_zero = head + cc * 16;  // any valid address for zero-filled rows
 #pragma unroll 4
-    for (int i = 0; i < 128 / kRowStep; ++i) {
-        const int r = r0 + i * kRowStep;
-        const int row = row0 + r;
-        const bool in = row < N;
-        const uint8_t *src = src_col + static_cast<size_t>(in ? row : 0) * (D * 2);
-        cp_async_16(dst + col + r * 128 + (((cc & 7) ^ (r & 7)) << 4), src, in ? 16u : 0u);
+        for (int i = 0; i < kIters; ++i) {
+            const bool in = row0 + r0 + i * kRowStep < N;
+            cp_async_16(((i & 1) ? d_odd : d_even) + i * kRowStep * 128,
+                        in ? src + i * kRowStep * (D * 2) : row_zero, in ? 16u : 0u);
+        }
     }
 }
 

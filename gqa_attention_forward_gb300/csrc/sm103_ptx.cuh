@@ -67,6 +67,11 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
+// Arrive on `bar` (counting as one expected arrival) once every cp.async this
+// thread issued so far has completed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 // Wait until at most N of this thread's committed groups are still in flight.
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
