@@ -39,27 +39,33 @@ struct Params {
     int inject_stall;  // test hook: the producer never loads Q
 };
 
-// Bounded wait on an mbarrier phase.  Gives up (returns false) when this CTA
-// or another CTA of the same launch has given up, or after timeout_ns; the
-// first to give up records ATTN_ERR_TIMEOUT.
+// Bounded wait on an mbarrier phase.  Spins on try_wait alone; every 256
+// spins it checks this CTA's abort flag, and once a millisecond has passed it
+// also checks whether another CTA of the launch gave up and whether timeout_ns
+// has run out (then it records ATTN_ERR_TIMEOUT and returns false).  Keeping
+// the global-memory check out of the tight loop matters: a waiting warp that
+// stalls on a global load notices the phase change late.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Params &p,
                                          volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) {
-            *abort_flag = 1;
-            return false;
-        }
-        if (global_timer_ns() - t0 > p.timeout_ns) {
-            *abort_flag = 1;
-            atomicCAS(&g_error_code, 0, static_cast<int>(ATTN_ERR_TIMEOUT));
-            atomicExch(&g_abort_seq, p.seq);
-            return false;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 255u) == 0) {
+            if (*abort_flag) return false;
+            const uint64_t dt = global_timer_ns() - t0;
+            if (dt > 1000000ull) {
+                if (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) {
+                    *abort_flag = 1;
+                    return false;
+                }
+                if (dt > p.timeout_ns) {
+                    *abort_flag = 1;
+                    atomicCAS(&g_error_code, 0, static_cast<int>(ATTN_ERR_TIMEOUT));
+                    atomicExch(&g_abort_seq, p.seq);
+                    return false;
+                }
+            }
         }
     }
 }
