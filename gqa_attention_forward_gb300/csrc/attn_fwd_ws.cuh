@@ -325,30 +325,41 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after();
                 __syncwarp();
                 uint32_t s[128];
+                const bool masked = kCausal ? (j == diag) : ((j + 1) * kBN > p.N);
+                if (!masked) {
+                    // Interior tile: each load also returns the max of its 32 columns.
+                    float mq[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    tmem_ld32(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q]));
-                tmem_ld_wait(s);
-                if (kCausal) {
-                    if (j == diag) {  // keep key c <= row r
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld32_max(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q]), mq[q]);
+                    tmem_ld_wait(s, mq);
+                    m_top = fmaxf(m_top, fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3])));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld32(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q]));
+                    tmem_ld_wait(s);
+                    if (kCausal) {  // diagonal tile: keep key c <= row r
 #pragma unroll
                         for (int cc = 0; cc < 128; ++cc)
                             if (cc > r) s[cc] = __float_as_uint(-INFINITY);
+                    } else {  // ragged last tile: keys >= N are absent
+                        const int lim = p.N - j * kBN;
+#pragma unroll
+                        for (int cc = 0; cc < 128; ++cc)
+                            if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
                     }
-                } else if ((j + 1) * kBN > p.N) {  // ragged last tile: keys >= N are absent
-                    const int lim = p.N - j * kBN;
+                    float mx[8];  // eight independent chains of 3-input max
 #pragma unroll
-                    for (int cc = 0; cc < 128; ++cc)
-                        if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
+                    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(u2f(s[2 * k]), u2f(s[2 * k + 1]));
+#pragma unroll
+                    for (int cc = 16; cc < 128; cc += 16)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            mx[k] = fmax3(mx[k], u2f(s[cc + 2 * k]), u2f(s[cc + 2 * k + 1]));
+                    m_top = fmaxf(m_top, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                               fmaxf(mx[6], mx[7])));
                 }
-                float mx[8];  // eight independent chains of 3-input max
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(u2f(s[2 * k]), u2f(s[2 * k + 1]));
-#pragma unroll
-                for (int cc = 16; cc < 128; cc += 16)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], u2f(s[cc + 2 * k]), u2f(s[cc + 2 * k + 1]));
-                m_top = fmaxf(m_top, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 // Re-reference only when the max has grown by more than kRescaleLog2
                 // (in log2 units) since the last reference; otherwise P may exceed 1.
                 float alpha = 1.f;
