@@ -39,14 +39,15 @@ namespace gqa {
 constexpr int kWsThreads = 384;
 constexpr int kStagesWs = 4;
 constexpr uint32_t kWsTmemCols = 512;
-// A tile's probabilities are split into two input-type terms (P_hi + P_lo)
-// when some row's running sum, in units of its largest weight, is below this.
+// A warp's 32 rows of probabilities are split into two input-type terms
+// (P_hi + P_lo) when some row's running sum, in units of its largest weight,
+// is below this.
 constexpr float kSplitL = 16.f;
 // The probabilities are referenced to a stale row max until the true max
 // exceeds it by more than this many powers of two (P <= 2^8 meanwhile).
 constexpr float kRescaleLog2 = 8.f;
-constexpr uint32_t kRegsLow = 112;   // warps 0-3 after the hand-off
-constexpr uint32_t kRegsHigh = 192;  // softmax warpgroups after the hand-off (128*112 + 256*192 <= 384*168)
+constexpr uint32_t kRegsLow = 104;   // warps 0-3 after the hand-off
+constexpr uint32_t kRegsHigh = 200;  // softmax warpgroups after the hand-off (128*104 + 256*200 <= 384*168)
 
 template <int D>
 struct WsLayout {
@@ -385,15 +386,22 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
                 const float2 sum2 = fadd2(acc[0], acc[1]);
                 l = l * alpha + (sum2.x + sum2.y);
-                // Split P = P_hi + P_lo for the whole tile when some row of the
-                // warpgroup has its weight on few keys: its running sum relative to
-                // its largest weight 2^((m_top - m_ref) c) is below kSplitL.  The
-                // four warps agree through a named barrier.
+                // Split P = P_hi + P_lo for a warp's 32 rows when one of them has its
+                // weight on few keys: its running sum relative to its largest weight
+                // 2^((m_top - m_ref) c) is below kSplitL.
                 const bool need = l * ex2_approx((m_ref - m_top) * c) < kSplitL;
-                if (lane == 0) split_flag(i, wq) = __any_sync(0xffffffffu, need) ? 1u : 0u;
-                else __any_sync(0xffffffffu, need);
-                named_bar_sync(1 + i, 128);
-                const bool split = (split_flag(i, 0) | split_flag(i, 1) | split_flag(i, 2) | split_flag(i, 3)) != 0;
+                // No warpgroup-wide agreement: a warp that does not split zeroes its
+                // P_lo columns, so the P_lo V pass, which the MMA warp issues when any
+                // of the four flags is set, adds nothing to its rows.
+                const bool split = __any_sync(0xffffffffu, need);
+                if (lane == 0) split_flag(i, wq) = split ? 1u : 0u;
+                if (!split) {
+                    uint32_t z[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) z[t] = 0u;
+                    tmem_st32(tS + 64, z);
+                    tmem_st32(tS + 96, z);
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t pk[16];
