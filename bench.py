@@ -170,6 +170,41 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
+KERNEL_SOURCES = ("gqa_attention_forward_gb300/csrc", "include/gqa_attn.h")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_ws_long_prefill_full.md")
+
+
+def kernel_source_digest() -> str:
+    """sha256 over the CUDA sources and the C header (file name + bytes, sorted)."""
+    import glob
+    import hashlib
+
+    files = sorted(glob.glob(os.path.join(ROOT, KERNEL_SOURCES[0], "*.cu")) +
+                   glob.glob(os.path.join(ROOT, KERNEL_SOURCES[0], "*.cuh")))
+    files.append(os.path.join(ROOT, KERNEL_SOURCES[1]))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload with the current kernel sources; otherwise None."""
+    try:
+        with open(TRAFFIC_PROFILE) as fh:
+            kv = dict(line.split(": ", 1) for line in fh.read().splitlines() if ": " in line)
+    except OSError:
+        return None
+    if kv.get("workload", "").strip() != workload:
+        return None
+    if kv.get("kernel_source_sha256", "").strip() != kernel_source_digest():
+        return None
+    return int(kv["dram_bytes_per_launch"])
+
+
 def to_dev(bits, dtype, device):
     import torch
 
@@ -267,6 +302,8 @@ def run_ours(args):
     d2h = ho.numel() * 2 + hl.numel() * 4
 
     if rank == 0:
+        # Q, K, V read once, O written once, LSE written once
+        algo_bytes = 2 * w.B * (2 * w.Hq + 2 * w.Hkv) * w.N * w.D + 4 * w.B * w.Hq * w.N
         peaks, peak_src = load_peaks()
         long_region = total_ms > 1000.0
         peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
@@ -284,7 +321,9 @@ def run_ours(args):
                              "inputs smaller than L2 (not flushed)",
                        "parallelism": f"replica x{world}"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": None,
+                         "unit": UNIT, "frac": round(achieved / peak, 4),
+                         "traffic": profiled_traffic(w.name),
+                         "algorithmic_bytes": algo_bytes,
                          "peak_source": f"{peak_src} "
                                         f"{'sustained' if long_region else 'burst'} bf16",
                          "kernel": "gqa::attn_fwd_ws_kernel", "kernel_ms": round(kern_ms, 4),
