@@ -72,6 +72,12 @@ def _declare(lib):
     lib.oracle_attention_rows.argtypes = [dp, lp, L, dp, dp, dp, dp, L, L, L, L, L,
                                           ctypes.c_double, ctypes.c_int, ctypes.c_int]
     lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_attention_kv.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L,
+                                        ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_attention_kv.restype = ctypes.c_int
+    lib.oracle_attention_rows_kv.argtypes = [dp, lp, L, dp, dp, dp, dp, L, L, L, L, L, L,
+                                             ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_attention_rows_kv.restype = ctypes.c_int
     return lib
 
 
@@ -94,44 +100,54 @@ def widen(bits: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def attention(q, k, v, scale: float, causal: bool, nthreads: int = 0, lib=None):
-    """O [B,Hq,N,D] and LSE [B,Hq,N] (natural log) for float64 q [B,Hq,N,D], k/v [B,Hkv,N,D].
+    """O [B,Hq,Nq,D] and LSE [B,Hq,Nq] (natural log) for float64 q [B,Hq,Nq,D] and
+    k/v [B,Hkv,Nk,D].  With Nq != Nk the causal mask is bottom-right aligned
+    (query i sees key j <= i + Nk - Nq).
 
     Returns (o, lse, threads_used)."""
     lib = lib or load_library()
     q, k, v = _f64(q), _f64(k), _f64(v)
-    B, Hq, N, D = q.shape
-    Hkv = k.shape[1]
-    if k.shape != (B, Hkv, N, D) or v.shape != k.shape:
-        raise ValueError("k, v must be [B, Hkv, N, D] matching q")
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Nk, D) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, Hkv, Nk, D] matching q")
     o = np.empty_like(q)
-    lse = np.empty((B, Hq, N), dtype=np.float64)
-    rc = lib.oracle_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                              B, Hq, Hkv, N, D, float(scale), int(bool(causal)), int(nthreads))
+    lse = np.empty((B, Hq, Nq), dtype=np.float64)
+    if Nq == Nk:
+        rc = lib.oracle_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                  B, Hq, Hkv, Nq, D, float(scale), int(bool(causal)),
+                                  int(nthreads))
+    else:
+        rc = lib.oracle_attention_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                     B, Hq, Hkv, Nq, Nk, D, float(scale), int(bool(causal)),
+                                     int(nthreads))
     if rc <= 0:
         raise RuntimeError("oracle_attention rejected its arguments")
     return o, lse, rc
 
 
 def attention_rows(q_rows, rows, k, v, Hq: int, scale: float, causal: bool,
-                   nthreads: int = 0, lib=None):
+                   nthreads: int = 0, lib=None, Nq: int | None = None):
     """Selected output rows only.
 
     q_rows [R, D] float64: the query row of each selected output row;
-    rows [R] int: flattened (b*Hq + hq)*N + i; k/v [B,Hkv,N,D] float64.
+    rows [R] int: flattened (b*Hq + hq)*Nq + i; k/v [B,Hkv,Nk,D] float64;
+    Nq: query rows per head (default Nk).
     Returns (o_rows [R, D], lse_rows [R], threads_used)."""
     lib = lib or load_library()
     q_rows, k, v = _f64(q_rows), _f64(k), _f64(v)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
-    B, Hkv, N, D = k.shape
+    B, Hkv, Nk, D = k.shape
+    Nq = Nk if Nq is None else int(Nq)
     R = rows.shape[0]
     if q_rows.shape != (R, D):
         raise ValueError("q_rows must be [len(rows), D]")
     o = np.empty((R, D), dtype=np.float64)
     lse = np.empty((R,), dtype=np.float64)
-    rc = lib.oracle_attention_rows(_ptr(q_rows), _ptr(rows, ctypes.c_longlong), R,
-                                   _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                   B, Hq, Hkv, N, D, float(scale), int(bool(causal)),
-                                   int(nthreads))
+    rc = lib.oracle_attention_rows_kv(_ptr(q_rows), _ptr(rows, ctypes.c_longlong), R,
+                                      _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      B, Hq, Hkv, Nq, Nk, D, float(scale), int(bool(causal)),
+                                      int(nthreads))
     if rc <= 0:
         raise RuntimeError("oracle_attention_rows rejected its arguments")
     return o, lse, rc

@@ -24,8 +24,15 @@
  * batch kept.  There is no tiling, no online rescaling and no fusion here:
  * one full score row per (b, q_head, i) in float64.
  *
- * Layouts (row-major, float64): q, o [B, Hq, N, D]; k, v [B, Hkv, N, D];
- * lse [B, Hq, N].
+ * Queries and keys may differ in number: Nq query rows attend over Nk keys
+ * (that page's kernel keeps separate query and key lengths).  The causal mask
+ * is then aligned at the bottom right: query i sees key j when
+ * j <= i + (Nk - Nq), so the query rows are the last Nq positions of an
+ * Nk-token sequence.  With Nq == Nk this is the square mask j <= i.  A causal
+ * call needs Nq <= Nk, so that every query row sees at least key 0.
+ *
+ * Layouts (row-major, float64): q, o [B, Hq, Nq, D]; k, v [B, Hkv, Nk, D];
+ * lse [B, Hq, Nq].
  */
 #include <math.h>
 #include <pthread.h>
@@ -33,17 +40,17 @@
 #include <unistd.h>
 
 /* One output row: (b, hq, i).  qi points at the D query values of the row;
- * kh, vh at the [N, D] key / value matrices of the row's kv head.  s is an
- * N-long scratch row. */
+ * kh, vh at the [N, D] key / value matrices of the row's kv head (N = Nk);
+ * off = Nk - Nq is the causal alignment offset.  s is an N-long scratch row. */
 static void attend_row(const double *qi, const double *kh, const double *vh,
                        long i, long N, long D, double scale, int causal,
-                       double *s, double *oi, double *lse_i)
+                       long off, double *s, double *oi, double *lse_i)
 {
     long j, d;
     /* scores with the mask applied as -inf */
     for (j = 0; j < N; ++j) {
         double acc = 0.0;
-        if (causal && j > i) {
+        if (causal && j > i + off) {
             s[j] = -INFINITY;
             continue;
         }
@@ -78,11 +85,11 @@ static void attend_row(const double *qi, const double *kh, const double *vh,
 
 typedef struct {
     const double *q_rows; /* [n_rows, D] query rows, in the order of rows[] */
-    const long long *rows; /* flattened (b*Hq + hq)*N + i for each row */
+    const long long *rows; /* flattened (b*Hq + hq)*Nq + i for each row */
     long n_rows;
     const double *k, *v;
     double *o_rows, *lse_rows;
-    long Hq, Hkv, N, D;
+    long Hq, Hkv, Nq, Nk, D;
     double scale;
     int causal;
     int tid, nthreads;
@@ -93,7 +100,7 @@ static void *run_rows(void *arg)
 {
     job_t *J = (job_t *)arg;
     long group = J->Hq / J->Hkv;
-    double *s = (double *)malloc(sizeof(double) * (size_t)J->N);
+    double *s = (double *)malloc(sizeof(double) * (size_t)J->Nk);
     if (!s) {
         J->failed = 1;
         return NULL;
@@ -101,14 +108,14 @@ static void *run_rows(void *arg)
     /* interleaved split: causal rows have uneven cost, neighbours even it out */
     for (long r = J->tid; r < J->n_rows; r += J->nthreads) {
         long long flat = J->rows[r];
-        long bh = (long)(flat / J->N); /* b*Hq + hq */
-        long i = (long)(flat % J->N);
+        long bh = (long)(flat / J->Nq); /* b*Hq + hq */
+        long i = (long)(flat % J->Nq);
         long kvh = bh / group; /* b*Hkv + hq / (Hq/Hkv) */
-        const double *kh = J->k + (size_t)kvh * J->N * J->D;
-        const double *vh = J->v + (size_t)kvh * J->N * J->D;
-        attend_row(J->q_rows + (size_t)r * J->D, kh, vh, i, J->N, J->D,
-                   J->scale, J->causal, s, J->o_rows + (size_t)r * J->D,
-                   J->lse_rows + r);
+        const double *kh = J->k + (size_t)kvh * J->Nk * J->D;
+        const double *vh = J->v + (size_t)kvh * J->Nk * J->D;
+        attend_row(J->q_rows + (size_t)r * J->D, kh, vh, i, J->Nk, J->D,
+                   J->scale, J->causal, J->Nk - J->Nq, s,
+                   J->o_rows + (size_t)r * J->D, J->lse_rows + r);
     }
     free(s);
     return NULL;
@@ -130,23 +137,24 @@ static int resolve_threads(int nthreads, long work)
 /*
  * Attention for a chosen set of output rows.
  *   q_rows   [n_rows, D]   the query row of each selected output row
- *   rows     [n_rows]      flattened index (b*Hq + hq)*N + i of each row
- *   k, v     [B, Hkv, N, D]
+ *   rows     [n_rows]      flattened index (b*Hq + hq)*Nq + i of each row
+ *   k, v     [B, Hkv, Nk, D]
  *   o_rows   [n_rows, D], lse_rows [n_rows]  (written)
- * Returns the number of threads used (> 0), or -1 on bad arguments or an
- * allocation failure.  nthreads <= 0 means one per online CPU.
+ * Returns the number of threads used (> 0), or -1 on bad arguments (also a
+ * causal call with Nq > Nk) or an allocation failure.  nthreads <= 0 means
+ * one per online CPU.
  */
-int oracle_attention_rows(const double *q_rows, const long long *rows,
-                          long n_rows, const double *k, const double *v,
-                          double *o_rows, double *lse_rows, long B, long Hq,
-                          long Hkv, long N, long D, double scale, int causal,
-                          int nthreads)
+int oracle_attention_rows_kv(const double *q_rows, const long long *rows,
+                             long n_rows, const double *k, const double *v,
+                             double *o_rows, double *lse_rows, long B, long Hq,
+                             long Hkv, long Nq, long Nk, long D, double scale,
+                             int causal, int nthreads)
 {
-    if (n_rows < 0 || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || N < 1 ||
-        D < 1)
+    if (n_rows < 0 || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || Nq < 1 ||
+        Nk < 1 || D < 1 || (causal && Nq > Nk))
         return -1;
     for (long r = 0; r < n_rows; ++r)
-        if (rows[r] < 0 || rows[r] >= (long long)B * Hq * N)
+        if (rows[r] < 0 || rows[r] >= (long long)B * Hq * Nq)
             return -1;
     int T = resolve_threads(nthreads, n_rows);
     pthread_t th[256];
@@ -154,7 +162,7 @@ int oracle_attention_rows(const double *q_rows, const long long *rows,
     int failed = 0;
     for (int t = 0; t < T; ++t) {
         job_t J = {q_rows, rows, n_rows, k, v, o_rows, lse_rows, Hq, Hkv,
-                   N, D, scale, causal, t, T, 0};
+                   Nq, Nk, D, scale, causal, t, T, 0};
         jobs[t] = J;
     }
     int started = 0;
@@ -175,21 +183,42 @@ int oracle_attention_rows(const double *q_rows, const long long *rows,
 }
 
 /*
- * Attention over every row: q, o [B, Hq, N, D]; k, v [B, Hkv, N, D];
- * lse [B, Hq, N].  Same return convention as oracle_attention_rows.
+ * Attention over every row: q, o [B, Hq, Nq, D]; k, v [B, Hkv, Nk, D];
+ * lse [B, Hq, Nq].  Same return convention as oracle_attention_rows_kv.
  */
-int oracle_attention(const double *q, const double *k, const double *v,
-                     double *o, double *lse, long B, long Hq, long Hkv,
-                     long N, long D, double scale, int causal, int nthreads)
+int oracle_attention_kv(const double *q, const double *k, const double *v,
+                        double *o, double *lse, long B, long Hq, long Hkv,
+                        long Nq, long Nk, long D, double scale, int causal,
+                        int nthreads)
 {
-    long n_rows = B * Hq * N;
+    long n_rows = B * Hq * Nq;
     long long *rows = (long long *)malloc(sizeof(long long) * (size_t)(n_rows > 0 ? n_rows : 1));
     if (!rows)
         return -1;
     for (long r = 0; r < n_rows; ++r)
         rows[r] = r;
-    int rc = oracle_attention_rows(q, rows, n_rows, k, v, o, lse, B, Hq, Hkv,
-                                   N, D, scale, causal, nthreads);
+    int rc = oracle_attention_rows_kv(q, rows, n_rows, k, v, o, lse, B, Hq,
+                                      Hkv, Nq, Nk, D, scale, causal, nthreads);
     free(rows);
     return rc;
+}
+
+/* Square problems (Nq == Nk == N): the two entry points above with N twice. */
+int oracle_attention_rows(const double *q_rows, const long long *rows,
+                          long n_rows, const double *k, const double *v,
+                          double *o_rows, double *lse_rows, long B, long Hq,
+                          long Hkv, long N, long D, double scale, int causal,
+                          int nthreads)
+{
+    return oracle_attention_rows_kv(q_rows, rows, n_rows, k, v, o_rows,
+                                    lse_rows, B, Hq, Hkv, N, N, D, scale,
+                                    causal, nthreads);
+}
+
+int oracle_attention(const double *q, const double *k, const double *v,
+                     double *o, double *lse, long B, long Hq, long Hkv,
+                     long N, long D, double scale, int causal, int nthreads)
+{
+    return oracle_attention_kv(q, k, v, o, lse, B, Hq, Hkv, N, N, D, scale,
+                               causal, nthreads);
 }

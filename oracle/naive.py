@@ -13,19 +13,22 @@ import math
 
 
 def attention_naive(q, k, v, scale, causal):
-    """q [B][Hq][N][D], k/v [B][Hkv][N][D] nested sequences of floats.
+    """q [B][Hq][Nq][D], k/v [B][Hkv][Nk][D] nested sequences of floats.
 
-    Returns (o [B][Hq][N][D], lse [B][Hq][N]) as nested lists of floats."""
-    B, Hq, N, D = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
-    Hkv = len(k[0])
+    The query rows are the last Nq positions of the Nk keys' sequence, so the
+    causal mask lets row i see keys 0 .. i + Nk - Nq.
+    Returns (o [B][Hq][Nq][D], lse [B][Hq][Nq]) as nested lists of floats."""
+    B, Hq, Nq, D = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
+    Hkv, Nk = len(k[0]), len(k[0][0])
     group = Hq // Hkv
-    o = [[[[0.0] * D for _ in range(N)] for _ in range(Hq)] for _ in range(B)]
-    lse = [[[0.0] * N for _ in range(Hq)] for _ in range(B)]
+    o = [[[[0.0] * D for _ in range(Nq)] for _ in range(Hq)] for _ in range(B)]
+    lse = [[[0.0] * Nq for _ in range(Hq)] for _ in range(B)]
     for b in range(B):
         for h in range(Hq):
             hk = h // group
-            for i in range(N):
-                allowed = [j for j in range(N) if not (causal and j > i)]
+            for i in range(Nq):
+                position = i + (Nk - Nq)  # of query row i within the key sequence
+                allowed = [j for j in range(Nk) if not (causal and j > position)]
                 w = {}
                 for j in allowed:
                     dot = math.fsum(q[b][h][i][d] * k[b][hk][j][d] for d in range(D))

@@ -242,6 +242,87 @@ def pin_torch_sdpa(att):
         _close(o, t.numpy(), tol=1e-11, what=f"torch sdpa causal={causal}")
 
 
+# ------------------------------------------------------------------ Nq != Nk
+# A block of Nq query rows attending over Nk >= Nq keys: the queries are the last
+# Nq positions of the keys' sequence, so the causal mask is aligned at the bottom
+# right (row i sees keys j <= i + Nk - Nq).
+
+
+def _mask_bottom_right(nq, nk):
+    return np.tril(np.ones((nq, nk), dtype=bool), k=nk - nq)
+
+
+def pin_bottom_right_library(att):
+    """Nq < Nk against scipy softmax / logsumexp over an explicitly built
+    bottom-right mask; Nq = 1 (one new token) sees every key."""
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, D = 2, 4, 2, 16
+    for nq, nk in ((1, 45), (7, 45), (30, 31), (13, 200)):
+        q = _rand(rng, B, Hq, nq, D, std=2.0)
+        k = _rand(rng, B, Hkv, nk, D, std=2.0)
+        v = _rand(rng, B, Hkv, nk, D)
+        for causal in (True, False):
+            o, lse = att(q, k, v, 0.25, causal)
+            kk, vv = np.repeat(k, Hq // Hkv, axis=1), np.repeat(v, Hq // Hkv, axis=1)
+            s = 0.25 * np.einsum("bhid,bhjd->bhij", q, kk)
+            if causal:
+                s = np.where(_mask_bottom_right(nq, nk), s, -np.inf)
+            want = np.einsum("bhij,bhjd->bhid", softmax(s, axis=-1), vv)
+            _close(o, want, tol=1e-11, what=f"Nq={nq} Nk={nk} causal={causal} O")
+            _close(lse, logsumexp(s, axis=-1), what=f"Nq={nq} Nk={nk} causal={causal} LSE")
+
+
+def pin_chunk_suffix(att):
+    """A causal query block equals the last Nq rows of the square causal problem whose
+    queries are a prefix followed by that block (chunked prefill)."""
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, D = 1, 6, 2, 8
+    for nq, nk in ((5, 40), (17, 17 + 128), (1, 9)):
+        q_tail = _rand(rng, B, Hq, nq, D)
+        q_full = np.concatenate([_rand(rng, B, Hq, nk - nq, D), q_tail], axis=2)
+        k = _rand(rng, B, Hkv, nk, D)
+        v = _rand(rng, B, Hkv, nk, D)
+        o1, l1 = att(q_tail, k, v, 0.5, True)
+        o2, l2 = att(q_full, k, v, 0.5, True)
+        _close(o1, o2[:, :, nk - nq:], what=f"suffix O Nq={nq} Nk={nk}")
+        _close(l1, l2[:, :, nk - nq:], what=f"suffix LSE Nq={nq} Nk={nk}")
+
+
+def pin_naive_nonsquare(att):
+    """Tiny Nq < Nk inputs against the pure-Python triple loop."""
+    from oracle.naive import attention_naive
+
+    rng = np.random.default_rng(14)
+    q = _rand(rng, 1, 2, 3, 4)
+    k = _rand(rng, 1, 1, 8, 4)
+    v = _rand(rng, 1, 1, 8, 4)
+    for causal in (True, False):
+        o, lse = att(q, k, v, 0.6, causal)
+        on, ln = attention_naive(q.tolist(), k.tolist(), v.tolist(), 0.6, causal)
+        _close(o, np.array(on), what=f"naive Nq<Nk O causal={causal}")
+        _close(lse, np.array(ln), what=f"naive Nq<Nk LSE causal={causal}")
+
+
+def pin_torch_sdpa_nonsquare(att):
+    """torch float64 scaled_dot_product_attention with the bottom-right mask passed
+    as an explicit boolean attn_mask (its is_causal is top-left for Nq != Nk)."""
+    import torch
+
+    rng = np.random.default_rng(15)
+    B, Hq, Hkv, nq, nk, D = 2, 8, 2, 19, 77, 32
+    q = _rand(rng, B, Hq, nq, D)
+    k = _rand(rng, B, Hkv, nk, D)
+    v = _rand(rng, B, Hkv, nk, D)
+    scale = 1.0 / math.sqrt(D)
+    o, _ = att(q, k, v, scale, True)
+    t = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(np.repeat(k, 4, axis=1)),
+        torch.from_numpy(np.repeat(v, 4, axis=1)),
+        attn_mask=torch.from_numpy(_mask_bottom_right(nq, nk)), scale=scale)
+    _close(o, t.numpy(), tol=1e-11, what="torch sdpa bottom-right")
+
+
 ALL_PINS = [pin_zero_query, pin_identity_values, pin_library_softmax, pin_selection,
             pin_shift, pin_gqa_vs_mha, pin_permutation, pin_single_key, pin_causality,
-            pin_naive, pin_torch_sdpa]
+            pin_naive, pin_torch_sdpa, pin_bottom_right_library, pin_chunk_suffix,
+            pin_naive_nonsquare, pin_torch_sdpa_nonsquare]

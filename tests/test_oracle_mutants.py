@@ -15,7 +15,10 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
 MUTANTS = {
     "interleaved_groups": ("long kvh = bh / group;",
                            "long kvh = (bh / J->Hq) * J->Hkv + (bh % J->Hq) % J->Hkv;"),
-    "mask_off_by_one": ("if (causal && j > i) {", "if (causal && j > i + 1) {"),
+    "mask_off_by_one": ("if (causal && j > i + off) {", "if (causal && j > i + off + 1) {"),
+    "alignment_top_left": ("if (causal && j > i + off) {", "if (causal && j > i) {"),
+    "alignment_offset_sign": ("if (causal && j > i + off) {", "if (causal && j > i - off) {"),
+    "query_row_index_from_keys": ("long i = (long)(flat % J->Nq);", "long i = (long)(flat % J->Nk);"),
     "scale_dropped": ("s[j] = scale * acc;", "s[j] = acc;"),
     "max_dropped_from_lse": ("*lse_i = m + log(l);", "*lse_i = log(l);"),
     "lse_base2": ("*lse_i = m + log(l);", "*lse_i = m + log2(l);"),
@@ -24,7 +27,7 @@ MUTANTS = {
     "feature_index_reversed": ("acc += qi[d] * kh[j * D + d];",
                                "acc += qi[d] * kh[j * D + (D - 1 - d)];"),
     "keys_used_as_values": ("oi[d] += s[j] * vh[j * D + d];", "oi[d] += s[j] * kh[j * D + d];"),
-    "causal_mask_dropped": ("if (causal && j > i) {", "if (0 && j > i) {"),
+    "causal_mask_dropped": ("if (causal && j > i + off) {", "if (0 && j > i + off) {"),
 }
 
 
