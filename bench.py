@@ -70,9 +70,10 @@ def load_peaks():
 
 # ------------------------------------------------------------------ CPU oracle
 def row_flops(w, rows: np.ndarray) -> float:
-    """Counted FLOPs of the selected output rows: 4*D per allowed key."""
+    """Counted FLOPs of the selected output rows: 4*D per allowed key (query row i
+    of a causal block of N rows over Nk keys sees i + Nk - N + 1 keys)."""
     i = rows % w.N
-    keys = (i + 1) if w.causal else np.full_like(i, w.N)
+    keys = (i + w.n_keys - w.N + 1) if w.causal else np.full_like(i, w.n_keys)
     return float(4.0 * w.D * keys.sum())
 
 
@@ -97,7 +98,7 @@ class OracleSampler:
         q_rows = self.oracle.widen(self.q[rows], w.dtype)
         t0 = time.perf_counter()
         _, _, self.threads = self.oracle.attention_rows(q_rows, rows, self.k, self.v, w.Hq, w.scale,
-                                                        w.causal)
+                                                        w.causal, Nq=w.N)
         return row_flops(w, rows), time.perf_counter() - t0
 
 
@@ -230,12 +231,17 @@ def run_ours(args):
     lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     dcode = binding.ATTN_BF16 if w.dtype == "bf16" else binding.ATTN_F16
-    args_c = (w.B, w.Hq, w.Hkv, w.N, w.D, w.scale, w.causal, dcode)
+    square = w.n_keys == w.N
 
     def step():
-        st = binding.attn_fwd(q, k, v, o, lse, *args_c, stream)
+        if square:
+            st = binding.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.D, w.scale, w.causal,
+                                  dcode, stream)
+        else:
+            st = binding.attn_fwd_kv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
+                                     w.scale, w.causal, dcode, stream)
         if st != binding.ATTN_OK:
-            raise binding.AttnError(st, "attn_fwd")
+            raise binding.AttnError(st, "attn_fwd" if square else "attn_fwd_kv")
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -303,7 +309,8 @@ def run_ours(args):
 
     if rank == 0:
         # Q, K, V read once, O written once, LSE written once
-        algo_bytes = 2 * w.B * (2 * w.Hq + 2 * w.Hkv) * w.N * w.D + 4 * w.B * w.Hq * w.N
+        algo_bytes = (2 * w.B * w.D * (2 * w.Hq * w.N + 2 * w.Hkv * w.n_keys)
+                      + 4 * w.B * w.Hq * w.N)
         peaks, peak_src = load_peaks()
         long_region = total_ms > 1000.0
         peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
@@ -312,12 +319,14 @@ def run_ours(args):
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms / K, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded i.i.d. normal, see workloads.py)",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "D": w.D,
-                       "causal": w.causal,
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
+                       "Nk": w.n_keys, "D": w.D, "causal": w.causal,
                        "flops_per_step": w.flops,
-                       "flop_convention": "2*B*Hq*N^2*D causal, 4*B*Hq*N^2*D non-causal",
+                       "flop_convention": "2*B*Hq*N^2*D causal, 4*B*Hq*N^2*D non-causal "
+                                          "(N query rows over Nk keys: 4*B*Hq*D*(N*Nk - N^2/2) "
+                                          "causal, 4*B*Hq*D*N*Nk non-causal)",
                        "l2": "inputs larger than L2 (no flush)" if
-                             (2 * w.B * (w.Hq + 2 * w.Hkv) * w.N * w.D) > 129e6 else
+                             (2 * w.B * w.D * (w.Hq * w.N + 2 * w.Hkv * w.n_keys)) > 129e6 else
                              "inputs smaller than L2 (not flushed)",
                        "parallelism": f"replica x{world}"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,

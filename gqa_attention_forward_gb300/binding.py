@@ -43,6 +43,8 @@ def load(path: str | None = None):
         vp, i = ctypes.c_void_p, ctypes.c_int
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, i, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, i, vp]
+        lib.attn_fwd_kv.restype = i
         lib.attn_status_str.argtypes = [i]
         lib.attn_status_str.restype = ctypes.c_char_p
         lib.attn_last_device_error.argtypes = [vp]
@@ -97,6 +99,14 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, causal, dtype, stream=Non
                         _stream_handle(stream))
 
 
+def attn_fwd_kv(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, stream=None) -> int:
+    """The C entry point with the same name; returns its status code."""
+    lib = load()
+    return lib.attn_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                           int(Hkv), int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
+                           _dtype_code(dtype), _stream_handle(stream))
+
+
 def attn_status_str(status: int) -> str:
     return load().attn_status_str(int(status)).decode()
 
@@ -115,14 +125,15 @@ def attn_version() -> int:
 
 def attention(q, k, v, causal: bool = True, scale: float | None = None, with_lse: bool = True,
               out=None, lse_out=None, stream=None):
-    """O (and LSE) for torch CUDA tensors q [B,Hq,N,D], k/v [B,Hkv,N,D] (fp16 or bf16).
+    """O (and LSE) for torch CUDA tensors q [B,Hq,Nq,D], k/v [B,Hkv,Nk,D] (fp16 or bf16).
 
-    torch allocates the outputs; the library computes them.  Launches on
-    ``stream`` (default: torch's current stream) and returns without waiting."""
+    With Nq != Nk the causal mask is bottom-right aligned (attn_fwd_kv).  torch
+    allocates the outputs; the library computes them.  Launches on ``stream``
+    (default: torch's current stream) and returns without waiting."""
     import torch
 
     B, Hq, N, D = q.shape
-    Hkv = k.shape[1]
+    Hkv, Nk = k.shape[1], k.shape[2]
     for t in (q, k, v):
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous [B, H, N, D]")
@@ -135,7 +146,10 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, with_lse
         scale = 1.0 / math.sqrt(D)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    st = attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, causal, q.dtype, stream)
+    if Nk == N:
+        st = attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, causal, q.dtype, stream)
+    else:
+        st = attn_fwd_kv(q, k, v, o, lse, B, Hq, Hkv, N, Nk, D, scale, causal, q.dtype, stream)
     if st != ATTN_OK:
         raise AttnError(st, f"attn_fwd ({attn_last_cuda_error()})")
     return o, lse

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = static_cast<int>(blockIdx.x / p.n_qtiles);  // b*Hq + hq
     const int kvh = bh / p.group;                               // b*Hkv + hq/(Hq/Hkv)
     const int q0 = q_tile * kBM;
-    const int n_kv = kCausal ? (q_tile + 1) : p.n_kv_tiles;
+    const int n_kv = kCausal ? causal_kv_tiles(q0, p.Nq, p.causal_off, p.n_kv_tiles) : p.n_kv_tiles;
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
@@ -123,12 +123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 2 && warp < 4) {
         // ---------------------------------------------------- loaders (warps 2, 3)
         const int ltid = threadIdx.x - 64;
-        const size_t head_bytes = static_cast<size_t>(p.N) * D * 2;
-        const uint8_t *kh = p.k + static_cast<size_t>(kvh) * head_bytes;
-        const uint8_t *vh = p.v + static_cast<size_t>(kvh) * head_bytes;
+        const size_t kv_head_bytes = static_cast<size_t>(p.Nk) * D * 2;
+        const uint8_t *kh = p.k + static_cast<size_t>(kvh) * kv_head_bytes;
+        const uint8_t *vh = p.v + static_cast<size_t>(kvh) * kv_head_bytes;
         LoadSignal sig;
         if (!p.inject_stall) {
-            load_tile<D>(sQ, p.q + static_cast<size_t>(bh) * head_bytes, q0, p.N, ltid);
+            load_tile<D>(sQ, p.q + static_cast<size_t>(bh) * p.Nq * D * 2, q0, p.Nq, ltid);
             sig.commit(q_full);
         }
         int stage = 0;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                load_tile<D>(sKV + stage * L::kTileBytes, t ? vh : kh, j * kBN, p.N, ltid);
+                load_tile<D>(sKV + stage * L::kTileBytes, t ? vh : kh, j * kBN, p.Nk, ltid);
                 sig.commit(kv_full(stage));
                 if (++stage == kStages) {
                     stage = 0;
@@ -228,13 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait(s);
             const int kv0 = j * kBN;
             if (kCausal) {
-                if (kv0 == q0) {  // diagonal tile: keep key c <= row r
+                const int lim0 = q0 + p.causal_off - kv0;  // row r sees keys c <= r + lim0 here
+                if (lim0 < kBN - 1) {
+                    const int lim = r + lim0;
 #pragma unroll
                     for (int cc = 0; cc < 128; ++cc)
-                        if (cc > r) s[cc] = __float_as_uint(-INFINITY);
+                        if (cc > lim) s[cc] = __float_as_uint(-INFINITY);
                 }
-            } else if (kv0 + kBN > p.N) {  // ragged last tile: keys >= N are absent
-                const int lim = p.N - kv0;
+            } else if (kv0 + kBN > p.Nk) {  // ragged last tile: keys >= Nk are absent
+                const int lim = p.Nk - kv0;
 #pragma unroll
                 for (int cc = 0; cc < 128; ++cc)
                     if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
@@ -290,13 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             const int row = q0 + r;
             const float inv_l = 1.f / l;
-            uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.N + row) * (D * 2);
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.Nq + row) * (D * 2);
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * q, o);
                 tmem_ld_wait(o);
-                if (row < p.N) {
+                if (row < p.Nq) {
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -307,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      w[4 * v + 3]);
                 }
             }
-            if (p.lse != nullptr && row < p.N)
-                p.lse[static_cast<size_t>(bh) * p.N + row] = (m * c + log2f(l)) * 0.6931471805599453f;
+            if (p.lse != nullptr && row < p.Nq)
+                p.lse[static_cast<size_t>(bh) * p.Nq + row] = (m * c + log2f(l)) * 0.6931471805599453f;
         }
     }
 
@@ -404,21 +406,23 @@ attn_status_t launch(int dev, int kid, const gqa::Params &prm, cudaStream_t stre
 
 extern "C" {
 
-attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
-                       int Hkv, int N, int D, float scale, int causal, attn_dtype_t dtype, void *stream) {
-    if (B < 0 || Hq < 0 || N < 0 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                          attn_dtype_t dtype, void *stream) {
+    if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
     if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_SHAPE;
     if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
     if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
-    if (B == 0 || Hq == 0 || N == 0) return ATTN_OK;
+    if (B == 0 || Hq == 0 || Nq == 0) return ATTN_OK;
+    if (Nk == 0 || (causal && Nq > Nk)) return ATTN_ERR_SHAPE;  // a query row would see no key
     if (!q || !k || !v || !o) return ATTN_ERR_NULL;
     auto misaligned = [](const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
     if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
         (lse && misaligned(lse, 4)))
         return ATTN_ERR_ALIGN;
     const long long BHq = static_cast<long long>(B) * Hq;
-    const int n_tiles = (N + gqa::kBN - 1) / gqa::kBN;
-    if (BHq * n_tiles > INT_MAX) return ATTN_ERR_SHAPE;
+    const int n_qtiles = (Nq + gqa::kBM - 1) / gqa::kBM;
+    if (BHq * n_qtiles > INT_MAX) return ATTN_ERR_SHAPE;
 
     int dev = 0;
     attn_status_t st = check_device(&dev);
@@ -431,12 +435,14 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
     prm.v = static_cast<const uint8_t *>(v);
     prm.o = o;
     prm.lse = lse;
-    prm.N = N;
+    prm.Nq = Nq;
+    prm.Nk = Nk;
+    prm.causal_off = Nk - Nq;
     prm.group = Hq / Hkv;
-    prm.n_qtiles = n_tiles;
-    prm.n_kv_tiles = n_tiles;
+    prm.n_qtiles = n_qtiles;
+    prm.n_kv_tiles = (Nk + gqa::kBN - 1) / gqa::kBN;
     prm.BHq = static_cast<int>(BHq);
-    prm.n_qblocks = (N + 255) / 256;
+    prm.n_qblocks = (Nq + 255) / 256;
     prm.n_items = static_cast<int>(BHq * prm.n_qblocks);
     prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     prm.seq = g_launch_seq.fetch_add(1);
@@ -454,6 +460,11 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
         case 6: return launch<128, true, false>(dev, kid, prm, s);
         default: return launch<128, true, true>(dev, kid, prm, s);
     }
+}
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                       int Hkv, int N, int D, float scale, int causal, attn_dtype_t dtype, void *stream) {
+    return attn_fwd_kv(q, k, v, o, lse, B, Hq, Hkv, N, N, D, scale, causal, dtype, stream);
 }
 
 const char *attn_status_str(attn_status_t status) {

@@ -90,12 +90,11 @@ __device__ __forceinline__ bool ws_item(const Params &p, int r, int &bh, int &qb
     return true;
 }
 
-// Key tiles visited by query tile i (0, 1) of block qb.
+// Key tiles visited by query tile i (0, 1) of block qb (never fewer for i = 1).
 template <bool kCausal>
 __device__ __forceinline__ int ws_tiles(const Params &p, int qb, int i) {
     if (!kCausal) return p.n_kv_tiles;
-    const int n = 2 * qb + 1 + i;  // up to and including the diagonal tile
-    return n < p.n_kv_tiles ? n : p.n_kv_tiles;
+    return causal_kv_tiles(qb * 256 + 128 * i, p.Nq, p.causal_off, p.n_kv_tiles);
 }
 
 template <int D, bool kBF16, bool kCausal>
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             // soon as they land (64 arrivals complete it).
             auto load_kv = [&](const uint8_t *head, int row0) -> bool {
                 if (!wait_bar(kv_empty(ring.s), ring.ph ^ 1u, p, abort_flag)) return false;
-                load_tile<D>(sKV + ring.s * L::kTileBytes, head, row0, p.N, ltid);
+                load_tile<D>(sKV + ring.s * L::kTileBytes, head, row0, p.Nk, ltid);
                 cp_async_arrive(kv_full(ring.s));
                 ring.next();
                 return true;
@@ -170,10 +169,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
                 int bh, qb;
                 if (!ws_item(p, r, bh, qb)) continue;
-                const size_t head_bytes = static_cast<size_t>(p.N) * D * 2;
-                const uint8_t *qh = p.q + static_cast<size_t>(bh) * head_bytes;
-                const uint8_t *kh = p.k + static_cast<size_t>(bh / p.group) * head_bytes;
-                const uint8_t *vh = p.v + static_cast<size_t>(bh / p.group) * head_bytes;
+                const size_t kv_head_bytes = static_cast<size_t>(p.Nk) * D * 2;
+                const uint8_t *qh = p.q + static_cast<size_t>(bh) * p.Nq * D * 2;
+                const uint8_t *kh = p.k + static_cast<size_t>(bh / p.group) * kv_head_bytes;
+                const uint8_t *vh = p.v + static_cast<size_t>(bh / p.group) * kv_head_bytes;
                 const int q0 = qb * 256;
                 const int n1 = ws_tiles<kCausal>(p, qb, 1);
                 // K_0 may land while the previous item still runs; the Q buffers
@@ -181,9 +180,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 if (!(ok = load_kv(kh, 0))) break;
                 if (!(ok = wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag))) break;
                 if (!p.inject_stall) {
-                    load_tile<D>(sQ, qh, q0, p.N, ltid);
+                    load_tile<D>(sQ, qh, q0, p.Nq, ltid);
                     cp_async_arrive(q_full(0));
-                    load_tile<D>(sQ + L::kTileBytes, qh, q0 + 128, p.N, ltid);
+                    load_tile<D>(sQ + L::kTileBytes, qh, q0 + 128, p.Nq, ltid);
                     cp_async_arrive(q_full(1));
                 }
                 ++items;
@@ -313,7 +312,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (!ws_item(p, rr, bh, qb)) continue;
             const int n = ws_tiles<kCausal>(p, qb, i);
             const int row0 = qb * 256 + 128 * i;  // first query row of this tile
-            const int diag = row0 / kBN;           // causal: the one masked key tile
             // m_ref: the max the probabilities are taken against (updated lazily);
             // m_top: the true running row max; l: running sum in units of 2^(m_ref*c).
             float m_ref = -INFINITY, m_top = -INFINITY, l = 0.f;
@@ -326,7 +324,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after();
                 __syncwarp();
                 uint32_t s[128];
-                const bool masked = kCausal ? (j == diag) : ((j + 1) * kBN > p.N);
+                // Causal: row r of this tile sees the tile's keys c <= r + lim0; the tile
+                // needs a mask unless every row sees all 128 of them.
+                const int lim0 = row0 + p.causal_off - j * kBN;
+                const bool masked = kCausal ? (lim0 < kBN - 1) : ((j + 1) * kBN > p.Nk);
                 if (!masked) {
                     // Interior tile: each load also returns the max of its 32 columns.
                     float mq[4];
@@ -340,12 +341,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     for (int q = 0; q < 4; ++q)
                         tmem_ld32(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q]));
                     tmem_ld_wait(s);
-                    if (kCausal) {  // diagonal tile: keep key c <= row r
+                    if (kCausal) {  // tile on the causal boundary: keep key c <= r + lim0
+                        const int lim = r + lim0;
 #pragma unroll
                         for (int cc = 0; cc < 128; ++cc)
-                            if (cc > r) s[cc] = __float_as_uint(-INFINITY);
-                    } else {  // ragged last tile: keys >= N are absent
-                        const int lim = p.N - j * kBN;
+                            if (cc > lim) s[cc] = __float_as_uint(-INFINITY);
+                    } else {  // ragged last tile: keys >= Nk are absent
+                        const int lim = p.Nk - j * kBN;
 #pragma unroll
                         for (int cc = 0; cc < 128; ++cc)
                             if (cc >= lim) s[cc] = __float_as_uint(-INFINITY);
@@ -445,13 +447,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             __syncwarp();
             const int row = row0 + r;
             const float inv_l = 1.f / l;  // l is in units of 2^(m_ref * c)
-            uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.N + row) * (D * 2);
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.Nq + row) * (D * 2);
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * q, o);
                 tmem_ld_wait(o);
-                if (row < p.N) {
+                if (row < p.Nq) {
                     uint32_t w[16];
 #pragma unroll
                     for (int t = 0; t < 16; ++t)
@@ -462,8 +464,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                      w[4 * v + 3]);
                 }
             }
-            if (p.lse != nullptr && row < p.N)
-                p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref * c + log2f(l)) * 0.6931471805599453f;
+            if (p.lse != nullptr && row < p.Nq)
+                p.lse[static_cast<size_t>(bh) * p.Nq + row] = (m_ref * c + log2f(l)) * 0.6931471805599453f;
             // O_i is read; the next item's first P_i V MMA waits for this warpgroup's p_full.
             tc_fence_before();
         }

@@ -20,18 +20,28 @@ constexpr int kBN = 128;  // key/value rows per tile
 __device__ int g_error_code;
 __device__ unsigned int g_abort_seq;
 
+// Key tiles a causal query tile visits: every tile up to the one holding the
+// last key visible to its last valid row (row < Nq).
+__device__ __forceinline__ int causal_kv_tiles(int row0, int Nq, int causal_off, int n_kv_tiles) {
+    const int last_row = (row0 + kBM - 1 < Nq - 1) ? row0 + kBM - 1 : Nq - 1;
+    const int n = (last_row + causal_off) / kBN + 1;
+    return n < n_kv_tiles ? n : n_kv_tiles;
+}
+
 struct Params {
-    const uint8_t *q;  // [B*Hq, N, D] elements of 2 bytes
-    const uint8_t *k;  // [B*Hkv, N, D]
-    const uint8_t *v;  // [B*Hkv, N, D]
+    const uint8_t *q;  // [B*Hq, Nq, D] elements of 2 bytes
+    const uint8_t *k;  // [B*Hkv, Nk, D]
+    const uint8_t *v;  // [B*Hkv, Nk, D]
     void *o;
     float *lse;
-    int N;
+    int Nq;          // query rows per head
+    int Nk;          // keys per head
+    int causal_off;  // Nk - Nq: under the causal mask query row i sees keys j <= i + causal_off
     int group;       // Hq / Hkv
-    int n_qtiles;    // ceil(N / kBM)
-    int n_kv_tiles;  // ceil(N / kBN)
+    int n_qtiles;    // ceil(Nq / kBM)
+    int n_kv_tiles;  // ceil(Nk / kBN)
     int BHq;         // B * Hq
-    int n_qblocks;   // ceil(N / 256): work items of the persistent kernel per head
+    int n_qblocks;   // ceil(Nq / 256): work items of the persistent kernel per head
     int n_items;     // BHq * n_qblocks
     float scale_log2;  // scale * log2(e)
     unsigned int seq;

@@ -35,6 +35,11 @@ class Workload:
     k_std: float = 1.0
     v_std: float = 1.0
     seed: int = 1234
+    Nk: int | None = None  # keys per head when it differs from the N query rows
+
+    @property
+    def n_keys(self) -> int:
+        return self.N if self.Nk is None else self.Nk
 
     @property
     def scale(self) -> float:
@@ -42,9 +47,12 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """Counted FLOPs: 4*B*Hq*N^2*D, halved for the causal mask."""
-        full = 4.0 * self.B * self.Hq * self.N * self.N * self.D
-        return full / 2.0 if self.causal else full
+        """Counted FLOPs: 4*B*Hq*N*Nk*D; with the causal mask the query block
+        drops the upper triangle of its last N columns: 4*B*Hq*D*(N*Nk - N^2/2),
+        which is 2*B*Hq*N^2*D for N == Nk."""
+        n, nk = float(self.N), float(self.n_keys)
+        pairs = n * nk - n * n / 2.0 if self.causal else n * nk
+        return 4.0 * self.B * self.Hq * self.D * pairs
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -60,6 +68,9 @@ WORKLOADS = {
                  seed=1237),
         Workload("tail_stress_causal_gqa_bf16_n2000", 8, 64, 8, 2000, 128, "bf16", True,
                  q_std=4.0, k_std=4.0, v_std=1.0, seed=1238),
+        # a 4096-token chunk of the long prefill over its 32768 keys (bottom-right mask)
+        Workload("chunked_prefill_causal_gqa_bf16_q4096_k32768", 1, 32, 8, 4096, 128, "bf16",
+                 True, seed=1239, Nk=32768),
     ]
 }
 ORDER = list(WORKLOADS)
@@ -86,13 +97,14 @@ def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def make_inputs(w: Workload, seed: int | None = None):
-    """q [B,Hq,N,D], k and v [B,Hkv,N,D] as uint16 storage words of w.dtype.
+    """q [B,Hq,N,D], k and v [B,Hkv,Nk,D] as uint16 storage words of w.dtype.
 
     Draw order is q, k, v from one numpy PCG64 generator seeded with w.seed."""
     rng = np.random.default_rng(w.seed if seed is None else seed)
     out = {}
-    for name, heads, std in (("q", w.Hq, w.q_std), ("k", w.Hkv, w.k_std), ("v", w.Hkv, w.v_std)):
-        x = rng.standard_normal((w.B, heads, w.N, w.D), dtype=np.float32)
+    for name, heads, rows, std in (("q", w.Hq, w.N, w.q_std), ("k", w.Hkv, w.n_keys, w.k_std),
+                                   ("v", w.Hkv, w.n_keys, w.v_std)):
+        x = rng.standard_normal((w.B, heads, rows, w.D), dtype=np.float32)
         if std != 1.0:
             x *= np.float32(std)
         out[name] = to_bits(x, w.dtype)

@@ -81,6 +81,26 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        int B, int Hq, int Hkv, int N, int D, float scale, int causal,
                        attn_dtype_t dtype, void *stream);
 
+/*
+ * attn_fwd_kv -- as attn_fwd, for Nq query rows attending over Nk keys (a
+ * block of new tokens over a longer key/value sequence, e.g. a chunk of a
+ * prefill or a decode step over a cache).  The derivation page's kernel
+ * ("从零开始写Qwen3", deepseek.csdn.net/6a3201f8..., section "FlashAttention")
+ * keeps the query and key lengths apart; this call does too.
+ *
+ * q, o   [B, Hq,  Nq, D];  k, v  [B, Hkv, Nk, D];  lse  [B, Hq, Nq] or NULL
+ * causal nonzero: the query rows are the last Nq positions of the Nk-long
+ *        sequence (bottom-right alignment): row i keeps keys j <= i + Nk - Nq.
+ *        With Nq == Nk this is attn_fwd's mask j <= i.
+ * Errors: as attn_fwd, plus ATTN_ERR_SHAPE when Nk == 0 while Nq > 0, or when
+ *        causal and Nq > Nk (some query row would see no key).  Nq == 0 is an
+ *        empty problem (nothing launched, ATTN_OK).
+ * attn_fwd(..., N, ...) is attn_fwd_kv(..., N, N, ...).
+ */
+attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+                          int causal, attn_dtype_t dtype, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *attn_status_str(attn_status_t status);
 

@@ -39,7 +39,8 @@ def oracle_full(w: workloads.Workload, x: dict):
 def oracle_rows(w: workloads.Workload, x: dict, rows: np.ndarray):
     q_rows = oracle.widen(x["q"].reshape(-1, w.D)[rows], w.dtype)
     o, lse, _ = oracle.attention_rows(q_rows, rows, oracle.widen(x["k"], w.dtype),
-                                      oracle.widen(x["v"], w.dtype), w.Hq, w.scale, w.causal)
+                                      oracle.widen(x["v"], w.dtype), w.Hq, w.scale, w.causal,
+                                      Nq=w.N)
     return o, lse
 
 

@@ -98,3 +98,36 @@ def test_oracle_is_not_on_the_product_path():
 def test_ctypes_signature_matches_header(lib):
     assert lib.attn_fwd.restype is ctypes.c_int
     assert len(lib.attn_fwd.argtypes) == 14
+    assert lib.attn_fwd_kv.restype is ctypes.c_int
+    assert len(lib.attn_fwd_kv.argtypes) == 15
+
+
+def _kv(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=4, Hkv=2, Nq=16, Nk=48, D=128,
+             scale=0.1, causal=1, dtype=1)
+    a.update(over)
+    return binding.attn_fwd_kv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"],
+                               a["Hkv"], a["Nq"], a["Nk"], a["D"], a["scale"], a["causal"],
+                               a["dtype"], None)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(Nq=49), 2),              # causal: rows 0 .. Nq-Nk-1 would see no key
+    (dict(Nk=0), 2),               # queries over no keys
+    (dict(Nk=0, causal=0), 2),
+    (dict(Nq=-1), 2), (dict(Nk=-3), 2), (dict(Hq=6, Hkv=4), 2),
+    (dict(D=80), 3), (dict(dtype=3), 4), (dict(k=0), 1), (dict(o=FAKE + 4), 5),
+])
+def test_kv_argument_errors(lib, args, code):
+    st = _kv(lib, **args)
+    assert st == code, (args, binding.STATUS.get(st))
+
+
+def test_kv_empty_and_non_causal_longer_queries(lib):
+    assert _kv(lib, q=None, k=None, v=None, o=None, Nq=0) == 0
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this checks the no-device path")
+    # Nq > Nk is fine without the mask, and Nq == Nk is attn_fwd: both pass validation
+    assert _kv(lib, Nq=64, Nk=48, causal=0) == 8
+    assert _kv(lib, Nq=48, Nk=48) == 8

@@ -35,7 +35,8 @@ def test_tail_stress_every_row():
 
 
 @pytest.mark.parametrize("name,count", [("noncausal_gqa_bf16_n4096", 3000),
-                                        ("long_prefill_causal_gqa_bf16_n32768", 1500)])
+                                        ("long_prefill_causal_gqa_bf16_n32768", 1500),
+                                        ("chunked_prefill_causal_gqa_bf16_q4096_k32768", 1500)])
 def test_workload_sampled_rows(name, count):
     """Full-size launch (the benchmarked configuration); oracle on a stratified row sample."""
     w = workloads.WORKLOADS[name]
@@ -203,3 +204,80 @@ def test_both_kernels_agree_on_pages_shape():
     assert float((o1.float() - o2.float()).abs().max()) <= 2e-3
     assert float((l1 - l2).abs().max()) <= 1e-4 * max(1.0, float(l1.abs().max()))
     assert torch.isfinite(o1).all()
+
+
+# ------------------------------------------------------------------ Nq != Nk
+KV_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, D, dtype, causal, qk_std
+    (1, 4, 2, 1, 300, 128, "bf16", True, 1.0),      # one new token over a cache
+    (2, 8, 2, 7, 4096, 128, "bf16", True, 1.0),
+    (2, 8, 2, 100, 1000, 128, "f16", True, 1.0),    # offset 900: two masked key tiles
+    (1, 4, 4, 256, 320, 64, "bf16", True, 1.0),     # offset 64
+    (1, 2, 1, 129, 256, 128, "f16", True, 1.0),     # offset 127, ragged query tile
+    (1, 8, 1, 384, 385, 128, "f16", True, 1.0),     # offset 1
+    (1, 2, 2, 600, 730, 128, "bf16", True, 4.0),    # near-one-hot rows
+    (2, 4, 2, 300, 70, 128, "bf16", False, 1.0),    # more queries than keys, no mask
+    (1, 6, 3, 90, 1000, 64, "f16", False, 2.0),
+]
+
+
+def _kv_workload(shape):
+    B, Hq, Hkv, Nq, Nk, D, dtype, causal, std = shape
+    return workloads.Workload("kv", B, Hq, Hkv, Nq, D, dtype, causal, q_std=std, k_std=std,
+                              seed=zlib.crc32(repr(shape).encode()) & 0xFFFF, Nk=Nk)
+
+
+@pytest.mark.parametrize("shape", KV_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_kv_shapes(shape):
+    """Nq query rows over Nk keys (bottom-right causal mask), every row against the oracle."""
+    w = _kv_workload(shape)
+    x = workloads.make_inputs(w)
+    o, lse = run_gpu(w, x)
+    assert tuple(o.shape) == (w.B, w.Hq, w.N, w.D) and tuple(lse.shape) == (w.B, w.Hq, w.N)
+    ro, rl = oracle_full(w, x)
+    err = assert_parity(w, _np(o), _np(lse), ro, rl, str(shape))
+    print(f"{shape}: max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
+
+
+@pytest.mark.parametrize("shape", KV_SHAPES[::2], ids=lambda s: "x".join(map(str, s)))
+def test_tile_kernel_kv_shapes(shape, tile_kernel):
+    test_kv_shapes(shape)
+
+
+def test_kv_with_equal_lengths_is_attn_fwd():
+    """attn_fwd_kv with Nq == Nk runs the same computation as attn_fwd: identical bits."""
+    import torch
+
+    w = workloads.Workload("eq", 1, 4, 2, 333, 128, "bf16", True, seed=21)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    l1 = torch.empty((1, 4, 333), dtype=torch.float32, device="cuda")
+    l2 = torch.empty_like(l1)
+    s = torch.cuda.current_stream()
+    assert binding.attn_fwd(q, k, v, o1, l1, 1, 4, 2, 333, 128, w.scale, 1, q.dtype, s) == 0
+    assert binding.attn_fwd_kv(q, k, v, o2, l2, 1, 4, 2, 333, 333, 128, w.scale, 1, q.dtype, s) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_kv_chunked_prefill_matches_one_pass():
+    """Two causal chunks over a growing key prefix give the rows of one square pass
+    (each within tolerance of the oracle, and of each other)."""
+    import torch
+
+    w = workloads.Workload("full", 1, 8, 2, 700, 128, "bf16", True, seed=22)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o_full, l_full = binding.attention(q, k, v, causal=True, scale=w.scale)
+    cut = 300
+    o_a, l_a = binding.attention(q[:, :, :cut].contiguous(), k[:, :, :cut].contiguous(),
+                                 v[:, :, :cut].contiguous(), causal=True, scale=w.scale)
+    o_b, l_b = binding.attention(q[:, :, cut:].contiguous(), k, v, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    o_cat = torch.cat([o_a, o_b], dim=2)
+    l_cat = torch.cat([l_a, l_b], dim=2)
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o_cat), _np(l_cat), ro, rl, "chunked")
+    assert float((o_cat.float() - o_full.float()).abs().max()) <= 1.6e-2
+
