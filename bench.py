@@ -50,6 +50,8 @@ def parse_args():
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of a CUDA graph holding one step (launch-overhead path)")
     return ap.parse_args()
 
 
@@ -233,18 +235,38 @@ def run_ours(args):
     dcode = binding.ATTN_BF16 if w.dtype == "bf16" else binding.ATTN_F16
     square = w.n_keys == w.N
 
-    def step():
+    def launch():
+        s_now = torch.cuda.current_stream(device)  # the capture stream while capturing
         if square:
             st = binding.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.D, w.scale, w.causal,
-                                  dcode, stream)
+                                  dcode, s_now)
         else:
             st = binding.attn_fwd_kv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
-                                     w.scale, w.causal, dcode, stream)
+                                     w.scale, w.causal, dcode, s_now)
         if st != binding.ATTN_OK:
             raise binding.AttnError(st, "attn_fwd" if square else "attn_fwd_kv")
 
+    step = launch
+    host_us = None
+    launch()  # the first call of a variant configures the kernel (and, in graph mode,
+    torch.cuda.synchronize()  # must come before the capture)
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            launch()
+        step = graph.replay
+
     for _ in range(max(args.warmup, 3)):
         step()
+    if not args.graph:
+        # host cost of one call through the Python binding (validation + launch), on
+        # warm calls queued back to back
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(20):
+            launch()
+        host_us = (time.perf_counter() - t0) / 20 * 1e6
+        torch.cuda.synchronize()
     st = binding.attn_last_device_error(stream)
     if st != binding.ATTN_OK:
         raise binding.AttnError(st, "warm-up")
@@ -341,6 +363,8 @@ def run_ours(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": K,
+            "launch": {"mode": "cuda_graph_replay" if args.graph else "direct",
+                       "host_us_per_call": None if host_us is None else round(host_us, 2)},
             "clocks": clock_info,
         }
         if not args.no_cpu_baseline:

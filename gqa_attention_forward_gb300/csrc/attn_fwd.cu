@@ -495,8 +495,13 @@ attn_status_t attn_last_device_error(void *stream) {
         return ATTN_ERR_LAUNCH;
     }
     if (code != 0) {
+        // Clear the error and the abort mark of the launch that gave up: a CUDA
+        // graph replays its launches with the sequence number they were captured
+        // with, and a stale mark would make every later replay exit at once.
         const int zero = 0;
+        const unsigned int no_seq = 0;  // sequence numbers start at 1
         e = cudaMemcpyToSymbol(gqa::g_error_code, &zero, sizeof(int));
+        if (e == cudaSuccess) e = cudaMemcpyToSymbol(gqa::g_abort_seq, &no_seq, sizeof(unsigned int));
         if (e != cudaSuccess) note_cuda_error(e, "cudaMemcpyToSymbol");
     }
     return static_cast<attn_status_t>(code);

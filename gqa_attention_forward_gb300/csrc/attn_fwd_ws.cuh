@@ -312,6 +312,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (!ws_item(p, rr, bh, qb)) continue;
             const int n = ws_tiles<kCausal>(p, qb, i);
             const int row0 = qb * 256 + 128 * i;  // first query row of this tile
+            // Causal: key tile j needs a mask unless its last key is visible to
+            // row0, i.e. from tile (row0 + Nk - Nq + 1) / 128 on.
+            const int first_masked = (row0 + p.causal_off + 1) / kBN;
             // m_ref: the max the probabilities are taken against (updated lazily);
             // m_top: the true running row max; l: running sum in units of 2^(m_ref*c).
             float m_ref = -INFINITY, m_top = -INFINITY, l = 0.f;
@@ -324,10 +327,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after();
                 __syncwarp();
                 uint32_t s[128];
-                // Causal: row r of this tile sees the tile's keys c <= r + lim0; the tile
-                // needs a mask unless every row sees all 128 of them.
-                const int lim0 = row0 + p.causal_off - j * kBN;
-                const bool masked = kCausal ? (lim0 < kBN - 1) : ((j + 1) * kBN > p.Nk);
+                const bool masked = kCausal ? (j >= first_masked) : ((j + 1) * kBN > p.Nk);
                 if (!masked) {
                     // Interior tile: each load also returns the max of its 32 columns.
                     float mq[4];
@@ -341,8 +341,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     for (int q = 0; q < 4; ++q)
                         tmem_ld32(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q]));
                     tmem_ld_wait(s);
-                    if (kCausal) {  // tile on the causal boundary: keep key c <= r + lim0
-                        const int lim = r + lim0;
+                    if (kCausal) {  // tile on the causal boundary: row r keeps keys c <= lim
+                        const int lim = r + row0 + p.causal_off - j * kBN;
 #pragma unroll
                         for (int cc = 0; cc < 128; ++cc)
                             if (cc > lim) s[cc] = __float_as_uint(-INFINITY);

@@ -70,7 +70,12 @@ typedef enum {
  * memory per call and keeps no pointer after the call returns.  o must not
  * overlap q, k or v.
  * Asynchrony: returns after the launch is queued on `stream`; results are
- * ready when the stream reaches that point.
+ * ready when the stream reaches that point.  The call never synchronises.
+ * CUDA graphs: a call can be captured into a CUDA graph (one kernel node; the
+ * node keeps the pointers, sizes and scale of the captured call).  The first
+ * call of each (D, dtype, causal) variant on a device sets the kernel's shared
+ * memory limit, which is not a stream operation: make one such call before
+ * capturing, as with any library that configures itself on first use.
  * Errors: argument errors are returned before anything is launched and leave
  * o and lse untouched.  An empty problem (B, Hq or N equal to 0) launches
  * nothing and returns ATTN_OK.  A wait inside the kernel that runs out of time
@@ -106,8 +111,11 @@ const char *attn_status_str(attn_status_t status);
 
 /*
  * Synchronises `stream`, then returns and clears the error word that kernels
- * of this library set on the current device (ATTN_OK if none).  A CUDA error
- * raised by the synchronisation itself is returned as ATTN_ERR_LAUNCH.
+ * of this library set on the current device (ATTN_OK if none), together with
+ * the mark that makes the other CTAs of a launch that gave up exit early.  A
+ * CUDA error raised by the synchronisation itself is returned as
+ * ATTN_ERR_LAUNCH.  Call it while no other launch of this library is running
+ * on the device.
  */
 attn_status_t attn_last_device_error(void *stream);
 

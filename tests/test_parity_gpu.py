@@ -281,3 +281,33 @@ def test_kv_chunked_prefill_matches_one_pass():
     assert_parity(w, _np(o_cat), _np(l_cat), ro, rl, "chunked")
     assert float((o_cat.float() - o_full.float()).abs().max()) <= 1.6e-2
 
+
+
+def test_cuda_graph_capture_and_replay():
+    """A call captured into a CUDA graph replays correctly, also on new inputs copied
+    into the captured buffers; replays keep working after an error was reported."""
+    import torch
+
+    w = workloads.WORKLOADS["pages_shape_causal_gqa_f16"]
+    x1 = workloads.make_inputs(w)
+    x2 = workloads.make_inputs(w, seed=w.seed + 100)
+    q, k, v = (to_device(x1[n], w.dtype) for n in "qkv")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+    binding.attention(q, k, v, causal=True, scale=w.scale, out=o, lse_out=lse)  # first use
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        binding.attention(q, k, v, causal=True, scale=w.scale, out=o, lse_out=lse)
+    o.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    ro, rl = oracle_full(w, x1)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "graph replay")
+    for name, t in zip("qkv", (q, k, v)):
+        t.copy_(to_device(x2[name], w.dtype))
+    graph.replay()
+    graph.replay()
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    ro2, rl2 = oracle_full(w, x2)
+    assert_parity(w, _np(o), _np(lse), ro2, rl2, "graph replay, new inputs")
