@@ -60,6 +60,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of the ranks' values (every rank gets it); x itself on one rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step_per_rank: float, steps: int, world: int, max_ms: float) -> float:
+    """Units all ranks processed over the slowest rank's time (weak scaling)."""
+    return world * flops_per_step_per_rank * steps / (max_ms / 1e3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -293,11 +310,8 @@ def run_ours(args):
         raise binding.AttnError(st, "timed region")
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = starts[0].elapsed_time(ends[-1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * w.flops * K / (total_ms / 1e3) / 1e12
+    total_ms = max_over_ranks(total_ms, device)
+    value = whole_job_tflops(w.flops, K, world, total_ms)
     kern_ms = float(np.mean(per_launch_ms))
     achieved = w.flops / (kern_ms / 1e3) / 1e12
 
@@ -322,10 +336,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / E
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, device)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * 2 + hl.numel() * 4
 
@@ -359,7 +370,7 @@ def run_ours(args):
                                         f"{'sustained' if long_region else 'burst'} bf16",
                          "kernel": "gqa::attn_fwd_ws_kernel", "kernel_ms": round(kern_ms, 4),
                          "frac_of_2250_nominal": round(achieved / 2250.0, 4)},
-            "e2e": {"value": round(world * w.flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
+            "e2e": {"value": round(whole_job_tflops(w.flops, 1, world, e2e_ms), 2), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": K,
