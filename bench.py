@@ -251,17 +251,27 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
     dcode = binding.ATTN_BF16 if w.dtype == "bf16" else binding.ATTN_F16
     square = w.n_keys == w.N
+    decode = w.entry == "attn_fwd_decode"
+    workspace, ws_bytes = None, 0
+    if decode:
+        st, ws_bytes = binding.attn_fwd_decode_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D)
+        if st != binding.ATTN_OK:
+            raise binding.AttnError(st, "attn_fwd_decode_workspace")
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
 
     def launch():
         s_now = torch.cuda.current_stream(device)  # the capture stream while capturing
-        if square:
+        if decode:
+            st = binding.attn_fwd_decode(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
+                                         w.scale, w.causal, dcode, workspace, ws_bytes, s_now)
+        elif square:
             st = binding.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.D, w.scale, w.causal,
                                   dcode, s_now)
         else:
             st = binding.attn_fwd_kv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
                                      w.scale, w.causal, dcode, s_now)
         if st != binding.ATTN_OK:
-            raise binding.AttnError(st, "attn_fwd" if square else "attn_fwd_kv")
+            raise binding.AttnError(st, w.entry if decode else ("attn_fwd" if square else "attn_fwd_kv"))
 
     step = launch
     host_us = None
@@ -346,7 +356,25 @@ def run_ours(args):
                       + 4 * w.B * w.Hq * w.N)
         peaks, peak_src = load_peaks()
         long_region = total_ms > 1000.0
-        peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
+        if decode:
+            # streams K and V once: bound by HBM bandwidth, not the tensor core
+            gbs = algo_bytes / (kern_ms / 1e3) / 1e9
+            roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "traffic": profiled_traffic(w.name), "algorithmic_bytes": algo_bytes,
+                        "peak_source": f"{peak_src} copy bandwidth",
+                        "kernel": "gqa::attn_fwd_decode_kernel"
+                                  + (" + gqa::attn_combine_kernel" if ws_bytes else ""),
+                        "kernel_ms": round(kern_ms, 4), "tflops": round(achieved, 2)}
+        else:
+            peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
+            roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                        "unit": UNIT, "frac": round(achieved / peak, 4),
+                        "traffic": profiled_traffic(w.name), "algorithmic_bytes": algo_bytes,
+                        "peak_source": f"{peak_src} "
+                                       f"{'sustained' if long_region else 'burst'} bf16",
+                        "kernel": "gqa::attn_fwd_ws_kernel", "kernel_ms": round(kern_ms, 4),
+                        "frac_of_2250_nominal": round(achieved / 2250.0, 4)}
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms / K, 4),
@@ -362,18 +390,11 @@ def run_ours(args):
                              (2 * w.B * w.D * (w.Hq * w.N + 2 * w.Hkv * w.n_keys)) > 129e6 else
                              "inputs smaller than L2 (not flushed)",
                        "parallelism": f"replica x{world}"},
-            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": UNIT, "frac": round(achieved / peak, 4),
-                         "traffic": profiled_traffic(w.name),
-                         "algorithmic_bytes": algo_bytes,
-                         "peak_source": f"{peak_src} "
-                                        f"{'sustained' if long_region else 'burst'} bf16",
-                         "kernel": "gqa::attn_fwd_ws_kernel", "kernel_ms": round(kern_ms, 4),
-                         "frac_of_2250_nominal": round(achieved / 2250.0, 4)},
+            "roofline": roofline,
             "e2e": {"value": round(whole_job_tflops(w.flops, 1, world, e2e_ms), 2), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": K,
+            "gpu_launches": K * (2 if ws_bytes else 1),
             "launch": {"mode": "cuda_graph_replay" if args.graph else "direct",
                        "host_us_per_call": None if host_us is None else round(host_us, 2)},
             "clocks": clock_info,

@@ -39,6 +39,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "attn_fwd_decode.cuh"
 #include "attn_fwd_ws.cuh"
 #include "gqa_attn.h"
 #include "kernel_common.cuh"
@@ -331,6 +332,7 @@ thread_local char t_last_cuda_error[256] = "";
 std::atomic<unsigned int> g_launch_seq{1};
 std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
 std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_force_splits{0};  // test hook: key splits of the packed kernel (0 = chosen)
 
 void note_cuda_error(cudaError_t e, const char *where) {
     std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", where, cudaGetErrorString(e));
@@ -368,6 +370,22 @@ attn_status_t check_device(int *dev_out) {
     return g_dev_state[dev] == 1 ? ATTN_OK : ATTN_ERR_NODEVICE;
 }
 
+// The first launch of a kernel instantiation on a device raises its dynamic
+// shared-memory limit (bit `kid` of the device's mask records it).
+template <typename K>
+attn_status_t set_smem_limit(int dev, int kid, K kern, int smem) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!(g_dev_smem_set[dev] >> kid & 1u)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "cudaFuncSetAttribute");
+            return ATTN_ERR_LAUNCH;
+        }
+        g_dev_smem_set[dev] |= 1u << kid;
+    }
+    return ATTN_OK;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 attn_status_t launch(int dev, int kid, const gqa::Params &prm, cudaStream_t stream) {
     const bool persistent = g_kernel_choice.load() == 0;
@@ -382,17 +400,7 @@ attn_status_t launch(int dev, int kid, const gqa::Params &prm, cudaStream_t stre
     } else {
         grid = static_cast<unsigned>(static_cast<long long>(prm.BHq) * prm.n_qtiles);
     }
-    {
-        std::lock_guard<std::mutex> lk(g_dev_mu);
-        if (!(g_dev_smem_set[dev] >> kid & 1u)) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) {
-                note_cuda_error(e, "cudaFuncSetAttribute");
-                return ATTN_ERR_LAUNCH;
-            }
-            g_dev_smem_set[dev] |= 1u << kid;
-        }
-    }
+    if (attn_status_t st = set_smem_limit(dev, kid, kern, smem); st != ATTN_OK) return st;
     kern<<<grid, threads, smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -402,18 +410,41 @@ attn_status_t launch(int dev, int kid, const gqa::Params &prm, cudaStream_t stre
     return ATTN_OK;
 }
 
-}  // namespace
+// Packed short-query kernel (one CTA per kv head, row tile and key split), then
+// the merge of the splits when there are several.
+template <int D, bool BF16, bool CAUSAL>
+attn_status_t launch_decode(int dev, int kid, const gqa::Params &prm, cudaStream_t stream) {
+    auto kern = gqa::attn_fwd_decode_kernel<D, BF16, CAUSAL>;
+    constexpr int smem = gqa::DecLayout<D>::kAlloc;
+    if (attn_status_t st = set_smem_limit(dev, 16 + kid, kern, smem); st != ATTN_OK) return st;
+    const long long grid = static_cast<long long>(prm.BHq / prm.group) * prm.n_mtiles * prm.n_splits;
+    kern<<<static_cast<unsigned>(grid), gqa::kDecThreads, smem, stream>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && prm.n_splits > 1) {
+        gqa::attn_combine_kernel<D, BF16><<<static_cast<unsigned>((prm.total_rows + 7) / 8), 256, 0, stream>>>(prm);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "kernel launch");
+        return ATTN_ERR_LAUNCH;
+    }
+    return ATTN_OK;
+}
 
-extern "C" {
-
-attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                          int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
-                          attn_dtype_t dtype, void *stream) {
+// Argument checks shared by the entry points and the fields of Params they
+// fill.  *empty is set for a problem with nothing to compute (B, Hq or Nq 0).
+attn_status_t prepare(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                      int Hkv, int Nq, int Nk, int D, float scale, int causal, attn_dtype_t dtype,
+                      gqa::Params &prm, int &dev, bool &empty) {
+    empty = false;
     if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
     if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_SHAPE;
     if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
     if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
-    if (B == 0 || Hq == 0 || Nq == 0) return ATTN_OK;
+    if (B == 0 || Hq == 0 || Nq == 0) {
+        empty = true;
+        return ATTN_OK;
+    }
     if (Nk == 0 || (causal && Nq > Nk)) return ATTN_ERR_SHAPE;  // a query row would see no key
     if (!q || !k || !v || !o) return ATTN_ERR_NULL;
     auto misaligned = [](const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
@@ -422,14 +453,12 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
         return ATTN_ERR_ALIGN;
     const long long BHq = static_cast<long long>(B) * Hq;
     const int n_qtiles = (Nq + gqa::kBM - 1) / gqa::kBM;
-    if (BHq * n_qtiles > INT_MAX) return ATTN_ERR_SHAPE;
+    if (BHq * n_qtiles > INT_MAX || BHq * Nq > INT_MAX) return ATTN_ERR_SHAPE;
 
-    int dev = 0;
     attn_status_t st = check_device(&dev);
     if (st != ATTN_OK) return st;
 
-    const bool bf16 = dtype == ATTN_BF16;
-    gqa::Params prm;
+    prm = gqa::Params{};
     prm.q = static_cast<const uint8_t *>(q);
     prm.k = static_cast<const uint8_t *>(k);
     prm.v = static_cast<const uint8_t *>(v);
@@ -448,6 +477,45 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
     prm.seq = g_launch_seq.fetch_add(1);
     prm.timeout_ns = g_timeout_ns.load();
     prm.inject_stall = g_inject_stall.load();
+    prm.rows_per_kv = prm.group * Nq;
+    prm.n_mtiles = (prm.rows_per_kv + gqa::kBM - 1) / gqa::kBM;
+    prm.total_rows = static_cast<int>(BHq * Nq);
+    prm.n_splits = 1;
+    prm.split_tiles = prm.n_kv_tiles;
+    return ATTN_OK;
+}
+
+// Key splits of the packed kernel: enough (kv head, row tile, split) CTAs for one
+// per SM, at least one key tile per split, and no more splits than `cap` (the
+// workspace's capacity in splits).  Fills n_splits and split_tiles.
+void plan_splits(gqa::Params &prm, int sms, long long cap) {
+    const long long tiles = static_cast<long long>(prm.BHq / prm.group) * prm.n_mtiles;
+    long long want = tiles >= sms ? 1 : sms / tiles;
+    if (const int forced = g_force_splits.load(); forced > 0) want = forced;
+    if (want > prm.n_kv_tiles) want = prm.n_kv_tiles;
+    if (want > cap) want = cap;
+    if (want < 1) want = 1;
+    prm.split_tiles = static_cast<int>((prm.n_kv_tiles + want - 1) / want);
+    prm.n_splits = (prm.n_kv_tiles + prm.split_tiles - 1) / prm.split_tiles;
+}
+
+size_t split_bytes(const gqa::Params &prm, int D) {
+    return static_cast<size_t>(prm.total_rows) * (D + 1) * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                          attn_dtype_t dtype, void *stream) {
+    gqa::Params prm;
+    int dev = 0;
+    bool empty = false;
+    attn_status_t st = prepare(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm, dev, empty);
+    if (st != ATTN_OK || empty) return st;
+    const bool bf16 = dtype == ATTN_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (kid) {
@@ -465,6 +533,53 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
                        int Hkv, int N, int D, float scale, int causal, attn_dtype_t dtype, void *stream) {
     return attn_fwd_kv(q, k, v, o, lse, B, Hq, Hkv, N, N, D, scale, causal, dtype, stream);
+}
+
+attn_status_t attn_fwd_decode_workspace(int B, int Hq, int Hkv, int Nq, int Nk, int D, size_t *bytes) {
+    if (bytes == nullptr) return ATTN_ERR_NULL;
+    *bytes = 0;
+    static const uint8_t dummy[16] = {};
+    gqa::Params prm;
+    int dev = 0;
+    bool empty = false;
+    // validate with stand-in pointers: only the sizes matter here
+    const void *fake = reinterpret_cast<const void *>((reinterpret_cast<uintptr_t>(dummy) + 15) & ~uintptr_t(15));
+    attn_status_t st = prepare(fake, fake, fake, const_cast<void *>(fake), nullptr, B, Hq, Hkv, Nq, Nk, D,
+                               1.f, 0, ATTN_BF16, prm, dev, empty);
+    if (st != ATTN_OK || empty) return st;
+    plan_splits(prm, g_dev_sms[dev], LLONG_MAX);
+    *bytes = prm.n_splits > 1 ? split_bytes(prm, D) * prm.n_splits : 0;
+    return ATTN_OK;
+}
+
+attn_status_t attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                              int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                              attn_dtype_t dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    gqa::Params prm;
+    int dev = 0;
+    bool empty = false;
+    attn_status_t st = prepare(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm, dev, empty);
+    if (st != ATTN_OK || empty) return st;
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_ERR_ALIGN;
+    const long long cap = workspace == nullptr ? 1 : static_cast<long long>(workspace_bytes / split_bytes(prm, D));
+    plan_splits(prm, g_dev_sms[dev], cap);
+    if (prm.n_splits > 1) {
+        prm.ws_o = static_cast<float *>(workspace);
+        prm.ws_lse = prm.ws_o + static_cast<size_t>(prm.n_splits) * prm.total_rows * D;
+    }
+    const bool bf16 = dtype == ATTN_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+    switch (kid) {
+        case 0: return launch_decode<64, false, false>(dev, kid, prm, s);
+        case 1: return launch_decode<64, false, true>(dev, kid, prm, s);
+        case 2: return launch_decode<64, true, false>(dev, kid, prm, s);
+        case 3: return launch_decode<64, true, true>(dev, kid, prm, s);
+        case 4: return launch_decode<128, false, false>(dev, kid, prm, s);
+        case 5: return launch_decode<128, false, true>(dev, kid, prm, s);
+        case 6: return launch_decode<128, true, false>(dev, kid, prm, s);
+        default: return launch_decode<128, true, true>(dev, kid, prm, s);
+    }
 }
 
 const char *attn_status_str(attn_status_t status) {
@@ -516,5 +631,7 @@ void attn_test_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(n
 void attn_test_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
 
 void attn_test_select_kernel(int which) { g_kernel_choice.store(which == 1 ? 1 : 0); }
+
+void attn_test_force_splits(int n_splits) { g_force_splits.store(n_splits > 0 ? n_splits : 0); }
 
 }  // extern "C"

@@ -47,6 +47,14 @@ struct Params {
     unsigned int seq;
     unsigned long long timeout_ns;
     int inject_stall;  // test hook: the producer never loads Q
+    // packed short-query path (attn_fwd_decode)
+    int rows_per_kv;   // Hq / Hkv * Nq query rows share one kv head (contiguous in Q)
+    int n_mtiles;      // ceil(rows_per_kv / kBM)
+    int n_splits;      // key splits per (kv head, row tile)
+    int split_tiles;   // key tiles per split
+    int total_rows;    // B * Hq * Nq
+    float *ws_o;       // [n_splits, total_rows, D] partial outputs (n_splits > 1)
+    float *ws_lse;     // [n_splits, total_rows] partial log-sum-exp
 };
 
 // Bounded wait on an mbarrier phase.  Spins on try_wait alone; every 256

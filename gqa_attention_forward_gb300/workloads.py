@@ -36,6 +36,7 @@ class Workload:
     v_std: float = 1.0
     seed: int = 1234
     Nk: int | None = None  # keys per head when it differs from the N query rows
+    entry: str = "attn_fwd"  # C entry point that computes it ("attn_fwd" or "attn_fwd_decode")
 
     @property
     def n_keys(self) -> int:
@@ -71,6 +72,14 @@ WORKLOADS = {
         # a 4096-token chunk of the long prefill over its 32768 keys (bottom-right mask)
         Workload("chunked_prefill_causal_gqa_bf16_q4096_k32768", 1, 32, 8, 4096, 128, "bf16",
                  True, seed=1239, Nk=32768),
+        # one new token over the long prefill's keys, and a batch of such steps:
+        # grouped-query packing and key splits (attn_fwd_decode)
+        Workload("decode_gqa_bf16_b1_q1_k32768", 1, 32, 8, 1, 128, "bf16", True, seed=1240,
+                 Nk=32768, entry="attn_fwd_decode"),
+        Workload("decode_gqa_bf16_b16_q1_k8192", 16, 32, 8, 1, 128, "bf16", True, seed=1241,
+                 Nk=8192, entry="attn_fwd_decode"),
+        Workload("short_chunk_gqa_bf16_q16_k32768", 1, 32, 8, 16, 128, "bf16", True, seed=1242,
+                 Nk=32768, entry="attn_fwd_decode"),
     ]
 }
 ORDER = list(WORKLOADS)

@@ -24,6 +24,8 @@
 #ifndef GQA_ATTN_H
 #define GQA_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -106,6 +108,45 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
                           int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
                           int causal, attn_dtype_t dtype, void *stream);
 
+/*
+ * attn_fwd_decode -- the same function as attn_fwd_kv, computed by a kernel
+ * for short query blocks over long key sequences (decode steps, small chunks).
+ *
+ * The Hq / Hkv query heads that share a kv head have adjacent rows, so their
+ * Hq/Hkv * Nq query rows are stacked into 128-row tiles and every K/V tile is
+ * read once per kv head (grouped-query packing).  The key range is cut into
+ * splits, one CTA each, so that few kv heads still fill the GPU; the splits'
+ * partial results are merged through their log-sum-exp by a second kernel
+ * (the online-softmax merge of the derivation page "从零开始写Qwen3",
+ * deepseek.csdn.net/6a3201f8..., section "在线softmax", applied across CTAs).
+ *
+ * Arguments as attn_fwd_kv, plus:
+ * workspace        device pointer, 16-byte aligned, or NULL; scratch for the
+ *                  partial results, owned by the caller, used by the two
+ *                  kernels this call queues on `stream` and free again once
+ *                  the stream has passed them.  Nothing in it needs to start
+ *                  at any value.
+ * workspace_bytes  its size.  The call uses as many splits as it wants and
+ *                  the workspace holds (attn_fwd_decode_workspace gives the
+ *                  size for all it wants); with NULL or too little for two
+ *                  splits it runs one split, which needs no workspace.
+ * Two calls that run at the same time must not share a workspace.
+ * Errors: as attn_fwd_kv; ATTN_ERR_ALIGN also for a misaligned workspace.
+ */
+attn_status_t attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+                              int causal, attn_dtype_t dtype, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/*
+ * Workspace bytes attn_fwd_decode uses for this problem on the current device
+ * when given enough (0 when it would run one split).  Writes *bytes; returns
+ * argument errors as attn_fwd_kv, ATTN_ERR_NULL for bytes == NULL and
+ * ATTN_ERR_NODEVICE without an sm_103 device.
+ */
+attn_status_t attn_fwd_decode_workspace(int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                        size_t *bytes);
+
 /* Static, human-readable name of a status code. */
 const char *attn_status_str(attn_status_t status);
 
@@ -146,6 +187,10 @@ void attn_test_inject_stall(int enable);
  *   Both compute the same operation; the second exists to cross-check the first.
  */
 void attn_test_select_kernel(int which);
+
+/* attn_test_force_splits: n > 0 makes attn_fwd_decode use n key splits (as far
+ * as the key tiles and the workspace allow); 0 restores its own choice. */
+void attn_test_force_splits(int n_splits);
 
 #ifdef __cplusplus
 }

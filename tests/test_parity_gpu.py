@@ -311,3 +311,81 @@ def test_cuda_graph_capture_and_replay():
     assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
     ro2, rl2 = oracle_full(w, x2)
     assert_parity(w, _np(o), _np(lse), ro2, rl2, "graph replay, new inputs")
+
+
+# ------------------------------------------------------------------ packed short queries
+DECODE_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, D, dtype, causal, qk_std, forced splits (0 = chosen)
+    (1, 32, 8, 1, 4096, 128, "bf16", True, 1.0, 0),     # one token over a cache
+    (2, 8, 2, 1, 1000, 128, "f16", True, 1.0, 3),       # ragged key tail
+    (1, 8, 1, 16, 3000, 128, "bf16", True, 1.0, 5),     # 8 heads x 16 rows = one full tile
+    (2, 4, 2, 7, 700, 64, "f16", True, 2.0, 0),
+    (1, 16, 2, 40, 900, 128, "bf16", True, 1.0, 4),     # 320 rows: tiles cut rows of a head
+    (1, 4, 4, 100, 100, 128, "bf16", True, 1.0, 2),     # square: some splits see no key
+    (1, 8, 2, 5, 2000, 128, "bf16", False, 1.0, 0),     # no mask
+    (2, 4, 1, 3, 520, 128, "bf16", True, 4.0, 3),       # near-one-hot rows
+    (1, 2, 1, 1, 1, 64, "f16", True, 1.0, 0),
+]
+
+
+@pytest.fixture
+def forced_splits():
+    lib = binding.load()
+    yield lib.attn_test_force_splits
+    lib.attn_test_force_splits(0)
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_decode_shapes(shape, forced_splits):
+    """attn_fwd_decode (grouped-query packing, key splits and their merge): every row
+    against the oracle."""
+    import torch
+
+    B, Hq, Hkv, Nq, Nk, D, dtype, causal, std, splits = shape
+    forced_splits(splits)
+    w = workloads.Workload("dec", B, Hq, Hkv, Nq, D, dtype, causal, q_std=std, k_std=std,
+                           seed=zlib.crc32(repr(shape).encode()) & 0xFFFF, Nk=Nk)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    o, lse = binding.attention_decode(q, k, v, causal=causal, scale=w.scale, workspace=ws)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    err = assert_parity(w, _np(o), _np(lse), ro, rl, str(shape))
+    print(f"{shape}: max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
+
+
+def test_decode_without_workspace_and_sizes():
+    """No workspace: one split, same function.  The size query asks for room for
+    several splits when few kv heads are in play, none when the row tiles fill the GPU."""
+    import torch
+
+    st, nbytes = binding.attn_fwd_decode_workspace(1, 32, 8, 1, 32768, 128)
+    assert st == binding.ATTN_OK and nbytes > 0
+    st, big = binding.attn_fwd_decode_workspace(512, 32, 8, 1, 4096, 128)
+    assert st == binding.ATTN_OK and big == 0
+    w = workloads.Workload("dec0", 1, 8, 2, 3, 128, "bf16", True, seed=31, Nk=1500)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 8, 3), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    assert binding.attn_fwd_decode(q, k, v, o, lse, 1, 8, 2, 3, 1500, 128, w.scale, 1, q.dtype,
+                                   None, 0, s) == binding.ATTN_OK
+    assert binding.attn_last_device_error(s) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "one split")
+
+
+def test_decode_agrees_with_kv_path():
+    """The packed kernel and the general kernel compute the same function."""
+    w = workloads.Workload("deckv", 2, 16, 4, 9, 128, "bf16", True, seed=32, Nk=2500)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o1, l1 = binding.attention(q, k, v, causal=True, scale=w.scale)
+    o2, l2 = binding.attention_decode(q, k, v, causal=True, scale=w.scale)
+    import torch
+
+    torch.cuda.synchronize()
+    assert float((o1.float() - o2.float()).abs().max()) <= 1.6e-2
+    assert float(((l1 - l2).abs() / l1.abs().clamp_min(1.0)).max()) <= 1e-4
