@@ -17,8 +17,8 @@ from . import build as _build
 ATTN_F16, ATTN_BF16 = 0, 1
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_HEADDIM",
           4: "ATTN_ERR_DTYPE", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_LAUNCH", 7: "ATTN_ERR_TIMEOUT",
-          8: "ATTN_ERR_NODEVICE"}
-ATTN_OK, ATTN_ERR_TIMEOUT = 0, 7
+          8: "ATTN_ERR_NODEVICE", 9: "ATTN_ERR_SCRATCH"}
+ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_SCRATCH = 0, 7, 9
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +48,9 @@ def load(path: str | None = None):
         lib.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, i,
                                         vp, ctypes.c_size_t, vp]
         lib.attn_fwd_decode.restype = i
+        lib.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float,
+                                                i, i, vp]
+        lib.attn_fwd_decode_noalloc.restype = i
         lib.attn_fwd_decode_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_fwd_decode_workspace.restype = i
         lib.attn_test_force_splits.argtypes = [i]
@@ -122,6 +125,15 @@ def attn_fwd_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype
                                int(Hkv), int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
                                _dtype_code(dtype), _ptr(workspace), int(workspace_bytes),
                                _stream_handle(stream))
+
+
+def attn_fwd_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
+                            stream=None) -> int:
+    """The C entry point with the same name; returns its status code."""
+    lib = load()
+    return lib.attn_fwd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                       int(Hq), int(Hkv), int(Nq), int(Nk), int(D), float(scale),
+                                       int(bool(causal)), _dtype_code(dtype), _stream_handle(stream))
 
 
 def attn_fwd_decode_workspace(B, Hq, Hkv, Nq, Nk, D):

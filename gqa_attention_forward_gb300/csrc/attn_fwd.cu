@@ -329,6 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace {
 
 thread_local char t_last_cuda_error[256] = "";
+
+// Scratch of attn_fwd_decode_noalloc: part of this module's device memory, so
+// no call allocates it.  Its address is looked up once per device.
+static __device__ __align__(256) float g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 std::atomic<unsigned int> g_launch_seq{1};
 std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
 std::atomic<int> g_inject_stall{0};
@@ -343,6 +347,7 @@ std::mutex g_dev_mu;
 int g_dev_state[kMaxDevices];      // 0 unknown, 1 sm_103, -1 other
 int g_dev_sms[kMaxDevices];        // multiprocessor count
 unsigned g_dev_smem_set[kMaxDevices];  // bit per kernel instantiation
+void *g_dev_scratch[kMaxDevices];      // address of g_noalloc_scratch on the device
 std::atomic<int> g_kernel_choice{0};   // 0 persistent warp-specialised, 1 one CTA per query tile
 
 attn_status_t check_device(int *dev_out) {
@@ -503,6 +508,28 @@ size_t split_bytes(const gqa::Params &prm, int D) {
     return static_cast<size_t>(prm.total_rows) * (D + 1) * sizeof(float);
 }
 
+// Launches the packed kernel (and the merge) with the splits planned in prm;
+// workspace holds the partial results when there are several.
+attn_status_t run_decode(gqa::Params &prm, int dev, int D, attn_dtype_t dtype, int causal, void *workspace,
+                         cudaStream_t s) {
+    if (prm.n_splits > 1) {
+        prm.ws_o = static_cast<float *>(workspace);
+        prm.ws_lse = prm.ws_o + static_cast<size_t>(prm.n_splits) * prm.total_rows * D;
+    }
+    const bool bf16 = dtype == ATTN_BF16;
+    const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+    switch (kid) {
+        case 0: return launch_decode<64, false, false>(dev, kid, prm, s);
+        case 1: return launch_decode<64, false, true>(dev, kid, prm, s);
+        case 2: return launch_decode<64, true, false>(dev, kid, prm, s);
+        case 3: return launch_decode<64, true, true>(dev, kid, prm, s);
+        case 4: return launch_decode<128, false, false>(dev, kid, prm, s);
+        case 5: return launch_decode<128, false, true>(dev, kid, prm, s);
+        case 6: return launch_decode<128, true, false>(dev, kid, prm, s);
+        default: return launch_decode<128, true, true>(dev, kid, prm, s);
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -563,23 +590,33 @@ attn_status_t attn_fwd_decode(const void *q, const void *k, const void *v, void 
     if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_ERR_ALIGN;
     const long long cap = workspace == nullptr ? 1 : static_cast<long long>(workspace_bytes / split_bytes(prm, D));
     plan_splits(prm, g_dev_sms[dev], cap);
+    return run_decode(prm, dev, D, dtype, causal, workspace, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                      int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+                                      int causal, attn_dtype_t dtype, void *stream) {
+    gqa::Params prm;
+    int dev = 0;
+    bool empty = false;
+    attn_status_t st = prepare(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm, dev, empty);
+    if (st != ATTN_OK || empty) return st;
+    plan_splits(prm, g_dev_sms[dev], LLONG_MAX);
+    void *scratch = nullptr;
     if (prm.n_splits > 1) {
-        prm.ws_o = static_cast<float *>(workspace);
-        prm.ws_lse = prm.ws_o + static_cast<size_t>(prm.n_splits) * prm.total_rows * D;
+        if (split_bytes(prm, D) * prm.n_splits > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH;
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (g_dev_scratch[dev] == nullptr) {
+            cudaError_t e = cudaGetSymbolAddress(&g_dev_scratch[dev], g_noalloc_scratch);
+            if (e != cudaSuccess) {
+                note_cuda_error(e, "cudaGetSymbolAddress");
+                g_dev_scratch[dev] = nullptr;
+                return ATTN_ERR_LAUNCH;
+            }
+        }
+        scratch = g_dev_scratch[dev];
     }
-    const bool bf16 = dtype == ATTN_BF16;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
-    switch (kid) {
-        case 0: return launch_decode<64, false, false>(dev, kid, prm, s);
-        case 1: return launch_decode<64, false, true>(dev, kid, prm, s);
-        case 2: return launch_decode<64, true, false>(dev, kid, prm, s);
-        case 3: return launch_decode<64, true, true>(dev, kid, prm, s);
-        case 4: return launch_decode<128, false, false>(dev, kid, prm, s);
-        case 5: return launch_decode<128, false, true>(dev, kid, prm, s);
-        case 6: return launch_decode<128, true, false>(dev, kid, prm, s);
-        default: return launch_decode<128, true, true>(dev, kid, prm, s);
-    }
+    return run_decode(prm, dev, D, dtype, causal, scratch, static_cast<cudaStream_t>(stream));
 }
 
 const char *attn_status_str(attn_status_t status) {
@@ -593,6 +630,7 @@ const char *attn_status_str(attn_status_t status) {
         case ATTN_ERR_LAUNCH: return "CUDA launch or driver call failed";
         case ATTN_ERR_TIMEOUT: return "in-kernel wait timed out";
         case ATTN_ERR_NODEVICE: return "no sm_103 device is current";
+        case ATTN_ERR_SCRATCH: return "problem needs more scratch than the fixed device buffer holds";
     }
     return "unknown status";
 }

@@ -48,7 +48,9 @@ typedef enum {
     ATTN_ERR_LAUNCH = 6,   /* a CUDA runtime / driver call failed (see attn_last_cuda_error) */
     ATTN_ERR_TIMEOUT = 7,  /* a bounded in-kernel wait ran out (reported by
                               attn_last_device_error) */
-    ATTN_ERR_NODEVICE = 8  /* no CUDA device of compute capability 10.3 is current */
+    ATTN_ERR_NODEVICE = 8, /* no CUDA device of compute capability 10.3 is current */
+    ATTN_ERR_SCRATCH = 9   /* attn_fwd_decode_noalloc: the problem needs more scratch
+                              than the library's fixed device buffer holds */
 } attn_status_t;
 
 /*
@@ -146,6 +148,39 @@ attn_status_t attn_fwd_decode(const void *q, const void *k, const void *v, void 
  */
 attn_status_t attn_fwd_decode_workspace(int B, int Hq, int Hkv, int Nq, int Nk, int D,
                                         size_t *bytes);
+
+/*
+ * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that cannot allocate
+ * device memory (an allocator-free runtime, a captured graph that must not own
+ * buffers, a call site that only receives q, k, v, o and lse).  The pages have
+ * no counterpart: their kernels keep everything on chip and need no scratch;
+ * the key splits of attn_fwd_decode do.
+ *
+ * Instead of a caller workspace the call uses a buffer that the library
+ * itself holds in device memory: ATTN_NOALLOC_SCRATCH_BYTES (16 MiB) per
+ * device, a static array of this library's module, so nothing is allocated
+ * on any call.  The split plan is the one attn_fwd_decode chooses with an
+ * unlimited workspace, so both calls give the same bits.  That plan needs at
+ * most (number of SMs) * 128 * (D + 1) * 4 bytes (10 MB on 152 SMs), so the
+ * buffer covers every problem on devices with up to 254 SMs; a plan that needs
+ * more (e.g. one forced by attn_test_force_splits) returns ATTN_ERR_SCRATCH
+ * before anything is launched.
+ *
+ * Arguments, layout, masks and errors: as attn_fwd_kv.
+ * Setup: the first call on a device looks up the buffer's address (not a
+ *   stream operation); make one call on each device before capturing calls
+ *   into a CUDA graph.
+ * Contents: nothing in the buffer needs to start at any value; each call
+ *   writes every part it reads.
+ * Races: all calls on one device share the buffer.  Calls queued on one
+ *   stream are ordered and safe; calls that can run at the same time (other
+ *   streams, concurrently replayed graphs) race on it and give undefined
+ *   results.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                      float scale, int causal, attn_dtype_t dtype, void *stream);
 
 /* Static, human-readable name of a status code. */
 const char *attn_status_str(attn_status_t status);
