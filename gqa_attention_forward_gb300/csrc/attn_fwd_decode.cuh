@@ -21,9 +21,12 @@
 //
 // Roles (256 threads): warps 2-3 load (cp.async, 4-stage ring), warp 1 issues
 // the MMAs (S = Q K^T and O += P V into TMEM), warps 4-7 run the softmax of
-// one row each and stage P through shared memory.  The O accumulator is
-// rescaled whenever a row's max grows, so the largest weight of a row is
-// exactly 1 and near one-hot rows keep their ratios through P's rounding.
+// one row each and stage P through shared memory.  S has two TMEM buffers and
+// P two shared-memory buffers, so the tensor core computes S(j+1) while the
+// softmax works on S(j), and the softmax waits for P(j-1) V only when it must
+// rescale O.  The O accumulator is rescaled whenever a row's max grows, so the
+// largest weight of a row is exactly 1 and near one-hot rows keep their
+// ratios through P's rounding.
 #pragma once
 #include "kernel_common.cuh"
 
@@ -31,17 +34,19 @@ namespace gqa {
 
 constexpr int kDecStages = 4;
 constexpr int kDecThreads = 256;
-constexpr uint32_t kDecTmemCols = 256;  // S [0, 128), O [128, 128 + D)
-constexpr uint32_t kDecTmemO = 128;
+constexpr uint32_t kDecTmemCols = 512;  // S0 [0, 128), S1 [128, 256), O [256, 256 + D)
+constexpr uint32_t kDecTmemO = 256;
+constexpr int kPBytes = 2 * kAtomBytes;  // one P buffer: 128 x 128 halves
 
 template <int D>
 struct DecLayout {
     static constexpr int kTileBytes = (D / 64) * kAtomBytes;
     static constexpr int kQ = 0;
     static constexpr int kKV = kQ + kTileBytes;
-    static constexpr int kP = kKV + kDecStages * kTileBytes;
-    static constexpr int kBar = kP + 2 * kAtomBytes;  // P: 128 x 128 halves
-    static constexpr int kNumBars = 1 + 2 * kDecStages + 4;
+    static constexpr int kP = kKV + kDecStages * kTileBytes;  // P0, P1
+    static constexpr int kBar = kP + 2 * kPBytes;
+    // q_full, kv_full[S], kv_empty[S], s_full[2], p_full, o_done[2], mma_done
+    static constexpr int kNumBars = 1 + 2 * kDecStages + 2 + 1 + 2 + 1;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kAlloc = kAbort + 4 + 1024;  // slack to align the base to 1024 B
@@ -105,10 +110,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint32_t q_full = bar0;
     auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
     auto kv_empty = [&](int s) { return bar0 + 8u * (1 + kDecStages + s); };
-    const uint32_t s_full = bar0 + 8u * (1 + 2 * kDecStages);
-    const uint32_t p_full = bar0 + 8u * (2 + 2 * kDecStages);
-    const uint32_t o_full = bar0 + 8u * (3 + 2 * kDecStages);
-    const uint32_t mma_done = bar0 + 8u * (4 + 2 * kDecStages);
+    auto s_full = [&](int b) { return bar0 + 8u * (1 + 2 * kDecStages + b); };
+    const uint32_t p_full = bar0 + 8u * (3 + 2 * kDecStages);
+    auto o_done = [&](int b) { return bar0 + 8u * (4 + 2 * kDecStages + b); };  // P_b V finished
+    const uint32_t mma_done = bar0 + 8u * (6 + 2 * kDecStages);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
 
@@ -119,9 +124,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mbar_init(kv_full(s), kLoaderThreads);
             mbar_init(kv_empty(s), 1);
         }
-        mbar_init(s_full, 1);
+        mbar_init(s_full(0), 1);
+        mbar_init(s_full(1), 1);
         mbar_init(p_full, kBM);
-        mbar_init(o_full, 1);
+        mbar_init(o_done(0), 1);
+        mbar_init(o_done(1), 1);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
@@ -149,21 +156,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         int stage = 0;
         uint32_t phase = 0;
-        bool ok = true;
-        for (int j = 0; j < n_kv && ok; ++j) {
-            for (int t = 0; t < 2; ++t) {
-                if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                load_tile<D>(sKV + stage * L::kTileBytes, t ? vh : kh, (kt0 + j) * kBN, p.Nk, ltid);
-                sig.commit(kv_full(stage));
-                if (++stage == kDecStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+        auto load = [&](const uint8_t *head, int j) -> bool {
+            if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) return false;
+            load_tile<D>(sKV + stage * L::kTileBytes, head, (kt0 + j) * kBN, p.Nk, ltid);
+            sig.commit(kv_full(stage));
+            if (++stage == kDecStages) {
+                stage = 0;
+                phase ^= 1u;
             }
-        }
+            return true;
+        };
+        // the MMA warp's order: K_0, K_1, then V_j, K_{j+2} for each j
+        bool ok = load(kh, 0) && (n_kv < 2 || load(kh, 1));
+        for (int j = 0; j < n_kv && ok; ++j) ok = load(vh, j) && (j + 2 >= n_kv || load(kh, j + 2));
         sig.announce<true>();
         cp_async_wait<0>();
     } else if (warp == 1) {
@@ -171,45 +176,58 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             // ---------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, kBM, kBN, false);
             constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, kBM, D, true);
-            const uint32_t tS = tmem, tO = tmem + kDecTmemO;
+            const uint32_t tO = tmem + kDecTmemO;
             bool ok = wait_bar(q_full, 0, p, abort_flag);
             tc_fence_after();
             int stage = 0;
             uint32_t phase = 0;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                if (!wait_bar(kv_full(stage), phase, p, abort_flag)) break;
+            auto next_stage = [&]() -> uint32_t {
+                const uint32_t st = sKV + stage * L::kTileBytes;
+                if (++stage == kDecStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                return st;
+            };
+            // S_b = Q K^T into TMEM buffer b (A = Q, B = K: both K-major, 128-byte swizzle)
+            auto qk = [&](int b) -> bool {
+                if (!wait_bar(kv_full(stage), phase, p, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t sK = sKV + stage * L::kTileBytes;
+                const int ks = stage;
+                const uint32_t sK = next_stage();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-                    mma_f16_ss(tS, sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(sK + koff, 16, 1024),
-                               idesc_qk, kk > 0);
+                    mma_f16_ss(tmem + 128u * b, sdesc_sw128(sQ + koff, 16, 1024),
+                               sdesc_sw128(sK + koff, 16, 1024), idesc_qk, kk > 0);
                 }
-                mma_commit(s_full);
-                mma_commit(kv_empty(stage));
-                if (++stage == kDecStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                if (!wait_bar(p_full, j & 1, p, abort_flag)) break;
+                mma_commit(s_full(b));
+                mma_commit(kv_empty(ks));
+                return true;
+            };
+            ok = ok && qk(0) && (n_kv < 2 || qk(1));
+            for (int j = 0; j < n_kv && ok; ++j) {
+                // O += P_b V_j   (A = P: K-major; B = V: MN-major, 64-wide chunks of D at
+                // LBO = one atom, 8-row groups of keys at SBO = 1024 B)
+                const int b = j & 1;
+                if (!(ok = wait_bar(p_full, j & 1, p, abort_flag))) break;
                 tc_fence_after();
-                if (!wait_bar(kv_full(stage), phase, p, abort_flag)) break;
+                if (!(ok = wait_bar(kv_full(stage), phase, p, abort_flag))) break;
                 tc_fence_after();
-                const uint32_t sV = sKV + stage * L::kTileBytes;
+                const int vs = stage;
+                const uint32_t sV = next_stage();
+                const uint32_t sPb = sP + b * kPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     const uint32_t poff = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-                    mma_f16_ss(tO, sdesc_sw128(sP + poff, 16, 1024),
+                    mma_f16_ss(tO, sdesc_sw128(sPb + poff, 16, 1024),
                                sdesc_sw128(sV + kk * 2048, kAtomBytes, 1024), idesc_pv,
                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(o_full);
-                mma_commit(kv_empty(stage));
-                if (++stage == kDecStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                mma_commit(o_done(b));
+                mma_commit(kv_empty(vs));
+                // S_b is free: its softmax read it before P_b was ready
+                if (j + 2 < n_kv) ok = qk(b);
             }
             mma_commit(mma_done);
             drain_bar(mma_done, 0, p);
@@ -225,19 +243,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // A key tile needs a mask when some row of the tile does not see all of it.
         const int tile_key_last = kCausal ? pos.lo + p.causal_off : p.Nk - 1;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_off, tO = tmem + kDecTmemO + lane_off;
+        const uint32_t tO = tmem + kDecTmemO + lane_off;
         const float c = p.scale_log2;
         float mrow = -INFINITY, l = 0.f;
         bool ok = true;
         const uint32_t prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
         for (int j = 0; j < n_kv; ++j) {
-            if (!__all_sync(0xffffffffu, wait_bar(s_full, j & 1, p, abort_flag))) {
+            const int b = j & 1;  // S, P buffer of this tile
+            if (!__all_sync(0xffffffffu, wait_bar(s_full(b), (j >> 1) & 1, p, abort_flag))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             __syncwarp();
             const int kv0 = (kt0 + j) * kBN;
+            const uint32_t tS = tmem + 128u * b + lane_off;
             uint32_t s[128];
             float mt;
             if (kv0 + kBN - 1 <= tile_key_last) {
@@ -271,14 +291,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             // -inf - -inf appears; its weights are then exactly 0
             const float m_use = m_new == -INFINITY ? 0.f : m_new;
             const float alpha = ex2_approx((mrow - m_use) * c);  // 0 while nothing was seen
-            if (j > 0) {
-                // P V_{j-1} must be done: it reads the P buffer and writes O.
-                if (!__all_sync(0xffffffffu, wait_bar(o_full, (j - 1) & 1, p, abort_flag))) {
+            if (j >= 2) {
+                // P_b is free once P_b V_{j-2} is done
+                if (!__all_sync(0xffffffffu, wait_bar(o_done(b), ((j - 2) >> 1) & 1, p, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (j > 0 && __any_sync(0xffffffffu, m_new > mrow)) {
+                // rescale O: P V_{j-1} must have finished writing it
+                if (!__all_sync(0xffffffffu, wait_bar(o_done(b ^ 1), ((j - 1) >> 1) & 1, p, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, m_new > mrow)) {
+                {
                     __syncwarp();
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
@@ -308,7 +335,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     acc[t & 1] = fadd2(acc[t & 1], e);
                     w[t] = pack2<kBF16>(e.x, e.y);
                 }
-                const uint32_t addr = prow + (ch >> 3) * kAtomBytes + (((ch & 7) ^ (r & 7)) << 4);
+                const uint32_t addr = prow + b * kPBytes + (ch >> 3) * kAtomBytes + (((ch & 7) ^ (r & 7)) << 4);
                 st_shared_v4(addr, w[0], w[1], w[2], w[3]);
             }
             const float2 sum2 = fadd2(acc[0], acc[1]);
@@ -318,7 +345,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mbar_arrive(p_full);
         }
         // ---------------------------------------------------- epilogue
-        if (ok && __all_sync(0xffffffffu, wait_bar(o_full, (n_kv - 1) & 1, p, abort_flag))) {
+        if (ok && __all_sync(0xffffffffu,
+                             wait_bar(o_done((n_kv - 1) & 1), ((n_kv - 1) >> 1) & 1, p, abort_flag))) {
             tc_fence_after();
             __syncwarp();
             const size_t R = base_row + m;  // flattened (b*Hq + hq)*Nq + i
