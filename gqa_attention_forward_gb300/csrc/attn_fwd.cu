@@ -426,8 +426,19 @@ attn_status_t launch_decode(int dev, int kid, const gqa::Params &prm, cudaStream
     kern<<<static_cast<unsigned>(grid), gqa::kDecThreads, smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && prm.n_splits > 1) {
-        gqa::attn_combine_kernel<D, BF16><<<static_cast<unsigned>((prm.total_rows + 7) / 8), 256, 0, stream>>>(prm);
-        e = cudaGetLastError();
+        // the merge waits for the split kernel inside (griddepcontrol.wait), so it
+        // may be launched as a programmatic dependent and overlap its tail
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((prm.total_rows + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gqa::attn_combine_kernel<D, BF16>, prm);
     }
     if (e != cudaSuccess) {
         note_cuda_error(e, "kernel launch");

@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int n_kv = kt1 > kt0 ? kt1 - kt0 : 0;
     const bool partial = p.n_splits > 1;
 
+    // Let the merge kernel (launched as a programmatic dependent) start its launch;
+    // it still waits for this whole grid before reading the workspace.
+    grid_launch_dependents();
     if (n_kv == 0) {
         // No key of this split is visible to these rows (only with several splits):
         // an empty piece, weight zero in the merge.
@@ -396,38 +399,65 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 }
 
 // Merges the n_splits pieces of every row: lse = log sum_s exp(lse_s) and
-// O = sum_s exp(lse_s - lse) * O_s.  One warp per row, D/32 columns per lane.
+// O = sum_s exp(lse_s - lse) * O_s.  One warp per row and D/32 columns per
+// lane; pieces go in batches of 16 whose log-sum-exps and partial rows are all
+// requested at once, with the running max and sum rebased between batches (the
+// same online merge), so up to 16 pieces cost one round trip to memory.  Launched as a
+// programmatic dependent of the split kernel: it waits for that grid's results
+// before reading them, so its launch overlaps the split kernel's tail.
 template <int D, bool kBF16>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const Params p) {
+__global__ void __launch_bounds__(128) attn_combine_kernel(const Params p) {
+    grid_dependency_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long R = static_cast<long long>(blockIdx.x) * 8 + warp;
+    const long long R = static_cast<long long>(blockIdx.x) * 4 + warp;
     if (R >= p.total_rows) return;
     constexpr int kPer = D / 32;
+    constexpr int kBatch = 16;  // pieces whose loads are in flight together
+    const int S = p.n_splits;
     const size_t stride = static_cast<size_t>(p.total_rows);
-    float mx = -INFINITY;
-    for (int s = 0; s < p.n_splits; ++s) mx = fmaxf(mx, p.ws_lse[s * stride + R]);
+    const float *col = p.ws_o + static_cast<size_t>(R) * D + lane * kPer;  // piece 0's columns
     float acc[kPer];
 #pragma unroll
     for (int d = 0; d < kPer; ++d) acc[d] = 0.f;
-    float sum = 0.f;
-    for (int s = 0; s < p.n_splits; ++s) {
-        const float ls = p.ws_lse[s * stride + R];
-        const float wgt = ls == -INFINITY ? 0.f : expf(ls - mx);
-        sum += wgt;
-        const float *src = p.ws_o + (s * stride + R) * D + lane * kPer;
-        if constexpr (kPer == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] += wgt * v.x;
-            acc[1] += wgt * v.y;
-            acc[2] += wgt * v.z;
-            acc[3] += wgt * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] += wgt * v.x;
-            acc[1] += wgt * v.y;
+    float mx = -INFINITY, sum = 0.f;  // running max and sum (lane-local weights, merged below)
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+        const int n = S - s0 < kBatch ? S - s0 : kBatch;
+        // the batch's log-sum-exps (lane t < n holds piece s0 + t) and partial rows,
+        // all requested before any of them is used
+        const float ls = lane < n ? p.ws_lse[(s0 + lane) * stride + R] : -INFINITY;
+        float v[kBatch][kPer];
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t)
+            if (t < n) {
+                const float *q = col + static_cast<size_t>(s0 + t) * stride * D;
+#pragma unroll
+                for (int d = 0; d < kPer; ++d) v[t][d] = q[d];
+            }
+        float bm = ls;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+        // rebase what was accumulated so far onto the new max (split 0 sees key 0,
+        // so the max is finite from the first batch on)
+        const float m_new = fmaxf(mx, bm);
+        const float scale_old = mx == -INFINITY ? 0.f : expf(mx - m_new);
+#pragma unroll
+        for (int d = 0; d < kPer; ++d) acc[d] *= scale_old;
+        sum *= scale_old;
+        mx = m_new;
+        const float wl = ls == -INFINITY ? 0.f : expf(ls - mx);
+        sum += wl;
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t) {
+            const float w = __shfl_sync(0xffffffffu, wl, t);
+            if (t < n) {
+#pragma unroll
+                for (int d = 0; d < kPer; ++d) acc[d] += w * v[t][d];
+            }
         }
     }
-    const float inv = 1.f / sum;  // split 0 holds key 0, which every row sees: sum >= 1
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float inv = 1.f / sum;
     uint32_t w[kPer / 2];
 #pragma unroll
     for (int t = 0; t < kPer / 2; ++t) w[t] = pack2<kBF16>(acc[2 * t] * inv, acc[2 * t + 1] * inv);

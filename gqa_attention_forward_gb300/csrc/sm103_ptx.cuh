@@ -231,6 +231,18 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: the dependent grid's griddepcontrol.wait
+// returns once every CTA of the grid it depends on has completed and its
+// memory operations are visible; launch_dependents lets that dependent grid be
+// launched before this one finishes.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

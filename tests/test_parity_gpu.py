@@ -325,6 +325,7 @@ DECODE_SHAPES = [
     (1, 8, 2, 5, 2000, 128, "bf16", False, 1.0, 0),     # no mask
     (2, 4, 1, 3, 520, 128, "bf16", True, 4.0, 3),       # near-one-hot rows
     (1, 2, 1, 1, 1, 64, "f16", True, 1.0, 0),
+    (1, 8, 2, 2, 6000, 128, "bf16", True, 1.0, 47),    # 47 pieces: three merge batches
 ]
 
 
