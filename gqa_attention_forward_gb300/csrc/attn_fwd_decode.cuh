@@ -152,17 +152,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const size_t kv_head_bytes = static_cast<size_t>(p.Nk) * D * 2;
         const uint8_t *kh = p.k + static_cast<size_t>(bkv) * kv_head_bytes;
         const uint8_t *vh = p.v + static_cast<size_t>(bkv) * kv_head_bytes;
-        LoadSignal sig;
+        // each thread's copies arrive on a tile's full barrier when they land
+        // (kLoaderThreads arrivals complete it), so the whole ring can be in flight
         if (!p.inject_stall) {
             load_tile<D>(sQ, p.q + base_row * (D * 2), m0, p.rows_per_kv, ltid);
-            sig.commit(q_full);
+            cp_async_arrive(q_full);
         }
         int stage = 0;
         uint32_t phase = 0;
         auto load = [&](const uint8_t *head, int j) -> bool {
             if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) return false;
             load_tile<D>(sKV + stage * L::kTileBytes, head, (kt0 + j) * kBN, p.Nk, ltid);
-            sig.commit(kv_full(stage));
+            cp_async_arrive(kv_full(stage));
             if (++stage == kDecStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -172,7 +173,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // the MMA warp's order: K_0, K_1, then V_j, K_{j+2} for each j
         bool ok = load(kh, 0) && (n_kv < 2 || load(kh, 1));
         for (int j = 0; j < n_kv && ok; ++j) ok = load(vh, j) && (j + 2 >= n_kv || load(kh, j + 2));
-        sig.announce<true>();
+        // every copy has landed before the CTA exits
+        cp_async_commit();
         cp_async_wait<0>();
     } else if (warp == 1) {
         if (lane == 0) {
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, kBM, D, true);
             const uint32_t tO = tmem + kDecTmemO;
             bool ok = wait_bar(q_full, 0, p, abort_flag);
+            fence_proxy_async_smem();  // cp.async data -> tensor core reads
             tc_fence_after();
             int stage = 0;
             uint32_t phase = 0;
@@ -195,6 +198,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             // S_b = Q K^T into TMEM buffer b (A = Q, B = K: both K-major, 128-byte swizzle)
             auto qk = [&](int b) -> bool {
                 if (!wait_bar(kv_full(stage), phase, p, abort_flag)) return false;
+                fence_proxy_async_smem();
                 tc_fence_after();
                 const int ks = stage;
                 const uint32_t sK = next_stage();
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 if (!(ok = wait_bar(p_full, j & 1, p, abort_flag))) break;
                 tc_fence_after();
                 if (!(ok = wait_bar(kv_full(stage), phase, p, abort_flag))) break;
+                fence_proxy_async_smem();
                 tc_fence_after();
                 const int vs = stage;
                 const uint32_t sV = next_stage();
