@@ -422,22 +422,25 @@ attn_status_t launch_decode(int dev, int kid, const gqa::Params &prm, cudaStream
     auto kern = gqa::attn_fwd_decode_kernel<D, BF16, CAUSAL>;
     constexpr int smem = gqa::DecLayout<D>::kAlloc;
     if (attn_status_t st = set_smem_limit(dev, 16 + kid, kern, smem); st != ATTN_OK) return st;
-    const long long grid = static_cast<long long>(prm.BHq / prm.group) * prm.n_mtiles * prm.n_splits;
-    kern<<<static_cast<unsigned>(grid), gqa::kDecThreads, smem, stream>>>(prm);
-    cudaError_t e = cudaGetLastError();
+    // Both kernels wait inside (griddepcontrol.wait) for the grid before them
+    // before touching global memory, so they are launched as programmatic
+    // dependents: their launch and set-up overlap the previous kernel's tail.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(prm.BHq / prm.group) * prm.n_mtiles *
+                                             prm.n_splits));
+    cfg.blockDim = dim3(gqa::kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
     if (e == cudaSuccess && prm.n_splits > 1) {
-        // the merge waits for the split kernel inside (griddepcontrol.wait), so it
-        // may be launched as a programmatic dependent and overlap its tail
-        cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>((prm.total_rows + 3) / 4));
         cfg.blockDim = dim3(128);
         cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, gqa::attn_combine_kernel<D, BF16>, prm);
     }
     if (e != cudaSuccess) {

@@ -85,12 +85,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int n_kv = kt1 > kt0 ? kt1 - kt0 : 0;
     const bool partial = p.n_splits > 1;
 
-    // Let the merge kernel (launched as a programmatic dependent) start its launch;
-    // it still waits for this whole grid before reading the workspace.
+    // This kernel and the merge are launched as programmatic dependents: let the
+    // next one start launching now (it waits for this grid before touching
+    // memory), and touch global memory only after the grid before this one is
+    // done (a previous call's merge may still read the workspace).
     grid_launch_dependents();
     if (n_kv == 0) {
         // No key of this split is visible to these rows (only with several splits):
         // an empty piece, weight zero in the merge.
+        grid_dependency_wait();
         if (warp >= 4) {
             const int m = m0 + (warp - 4) * 32 + lane;
             if (m < p.rows_per_kv) {
@@ -145,6 +148,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dependency_wait();  // the set-up above overlapped the previous kernel's tail
 
     if (warp >= 2 && warp < 4) {
         // ---------------------------------------------------- loaders (warps 2, 3)
@@ -412,6 +416,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // before reading them, so its launch overlaps the split kernel's tail.
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const Params p) {
+    grid_launch_dependents();  // the next call's split kernel may begin its set-up
     grid_dependency_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long R = static_cast<long long>(blockIdx.x) * 4 + warp;
