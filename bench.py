@@ -190,18 +190,19 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
-KERNEL_SOURCES = ("gqa_attention_forward_gb300/csrc", "include/gqa_attn.h")
+# the files the persistent prefill kernel (attn_fwd_ws_kernel) is compiled from
+KERNEL_SOURCES = ("gqa_attention_forward_gb300/csrc/attn_fwd_ws.cuh",
+                  "gqa_attention_forward_gb300/csrc/kernel_common.cuh",
+                  "gqa_attention_forward_gb300/csrc/sm103_ptx.cuh",
+                  "include/gqa_attn.h")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_ws_long_prefill_full.md")
 
 
 def kernel_source_digest() -> str:
-    """sha256 over the CUDA sources and the C header (file name + bytes, sorted)."""
-    import glob
+    """sha256 over the kernel's source files (file name + bytes, in a fixed order)."""
     import hashlib
 
-    files = sorted(glob.glob(os.path.join(ROOT, KERNEL_SOURCES[0], "*.cu")) +
-                   glob.glob(os.path.join(ROOT, KERNEL_SOURCES[0], "*.cuh")))
-    files.append(os.path.join(ROOT, KERNEL_SOURCES[1]))
+    files = [os.path.join(ROOT, f) for f in KERNEL_SOURCES]
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
