@@ -390,3 +390,29 @@ def test_decode_agrees_with_kv_path():
     torch.cuda.synchronize()
     assert float((o1.float() - o2.float()).abs().max()) <= 1.6e-2
     assert float(((l1 - l2).abs() / l1.abs().clamp_min(1.0)).max()) <= 1e-4
+
+
+def test_decode_timeout_is_reported_and_context_survives(forced_splits):
+    """The packed split kernel under a wait nothing satisfies (the Q load is skipped):
+    it records ATTN_ERR_TIMEOUT and returns; the next call is correct."""
+    import torch
+
+    lib = binding.load()
+    forced_splits(4)
+    w = workloads.Workload("dstall", 1, 8, 2, 2, 128, "bf16", True, seed=33, Nk=1500)
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    ws = torch.empty(8 << 20, dtype=torch.uint8, device="cuda")
+    try:
+        lib.attn_test_set_wait_timeout_ns(300_000_000)
+        lib.attn_test_inject_stall(1)
+        binding.attention_decode(q, k, v, causal=True, scale=w.scale, workspace=ws)
+        st = binding.attn_last_device_error(torch.cuda.current_stream())
+    finally:
+        lib.attn_test_inject_stall(0)
+        lib.attn_test_set_wait_timeout_ns(0)
+    assert st == binding.ATTN_ERR_TIMEOUT
+    o, lse = binding.attention_decode(q, k, v, causal=True, scale=w.scale, workspace=ws)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "decode after timeout")
