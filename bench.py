@@ -334,16 +334,28 @@ def run_ours(args):
     dq, dk, dv = (t.view(torch.int16).view(-1) for t in (q, k, v))
     do = o.view(torch.int16).view(-1)
     E = max(1, min(args.e2e_steps, K))
+
+    def e2e_step():
+        if decode:
+            dq.copy_(hq.view(-1), non_blocking=True)
+            dk.copy_(hk.view(-1), non_blocking=True)
+            dv.copy_(hv.view(-1), non_blocking=True)
+            step()
+            ho.copy_(do, non_blocking=True)
+            hl.copy_(lse.view(-1), non_blocking=True)
+            return
+        # one C-ABI call with host buffers: chunked copies in and out overlap the compute
+        st = binding.attn_fwd_host(hq, hk, hv, ho, hl, q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N,
+                                   w.n_keys, w.D, w.scale, w.causal, dcode, stream)
+        if st != binding.ATTN_OK:
+            raise binding.AttnError(st, "attn_fwd_host")
+
+    e2e_step()  # first call creates the library's copy streams
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E):
-        dq.copy_(hq.view(-1), non_blocking=True)
-        dk.copy_(hk.view(-1), non_blocking=True)
-        dv.copy_(hv.view(-1), non_blocking=True)
-        step()
-        ho.copy_(do, non_blocking=True)
-        hl.copy_(lse.view(-1), non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / E
@@ -394,7 +406,9 @@ def run_ours(args):
             "roofline": roofline,
             "e2e": {"value": round(whole_job_tflops(w.flops, 1, world, e2e_ms), 2), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4),
+                    "path": ("torch copies around attn_fwd_decode" if decode else
+                             "attn_fwd_host: pinned host buffers, chunked copies overlapping compute")},
             "gpu_launches": K * (2 if ws_bytes else 1),
             "launch": {"mode": "cuda_graph_replay" if args.graph else "direct",
                        "host_us_per_call": None if host_us is None else round(host_us, 2)},

@@ -51,6 +51,9 @@ def load(path: str | None = None):
         lib.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float,
                                                 i, i, vp]
         lib.attn_fwd_decode_noalloc.restype = i
+        lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                      ctypes.c_float, i, i, vp]
+        lib.attn_fwd_host.restype = i
         lib.attn_fwd_decode_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_fwd_decode_workspace.restype = i
         lib.attn_test_force_splits.argtypes = [i]
@@ -134,6 +137,17 @@ def attn_fwd_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causa
     return lib.attn_fwd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
                                        int(Hq), int(Hkv), int(Nq), int(Nk), int(D), float(scale),
                                        int(bool(causal)), _dtype_code(dtype), _stream_handle(stream))
+
+
+def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, B, Hq, Hkv, Nq, Nk, D,
+                  scale, causal, dtype, stream=None) -> int:
+    """The C entry point with the same name; returns its status code.  Host
+    arguments are CPU tensors (pinned for overlap), device arguments CUDA tensors."""
+    lib = load()
+    return lib.attn_fwd_host(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(lse_h), _ptr(q_d),
+                             _ptr(k_d), _ptr(v_d), _ptr(o_d), _ptr(lse_d), int(B), int(Hq), int(Hkv),
+                             int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
+                             _dtype_code(dtype), _stream_handle(stream))
 
 
 def attn_fwd_decode_workspace(B, Hq, Hkv, Nq, Nk, D):

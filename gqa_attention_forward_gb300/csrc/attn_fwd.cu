@@ -348,6 +348,18 @@ int g_dev_state[kMaxDevices];      // 0 unknown, 1 sm_103, -1 other
 int g_dev_sms[kMaxDevices];        // multiprocessor count
 unsigned g_dev_smem_set[kMaxDevices];  // bit per kernel instantiation
 void *g_dev_scratch[kMaxDevices];      // address of g_noalloc_scratch on the device
+
+// Streams and events of attn_fwd_host, created on the first call on a device and
+// kept for the life of the process (no memory is allocated per call).
+constexpr int kMaxChunks = 8;
+struct HostPipe {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[kMaxChunks] = {}, out[kMaxChunks] = {};
+    bool ready = false;
+};
+std::mutex g_pipe_mu;  // serialises the enqueueing of attn_fwd_host calls
+HostPipe g_pipe[kMaxDevices];
 std::atomic<int> g_kernel_choice{0};   // 0 persistent warp-specialised, 1 one CTA per query tile
 
 attn_status_t check_device(int *dev_out) {
@@ -544,6 +556,27 @@ attn_status_t run_decode(gqa::Params &prm, int dev, int D, attn_dtype_t dtype, i
     }
 }
 
+attn_status_t host_pipe(int dev, HostPipe *&pipe) {
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming);
+        for (int c = 0; c < kMaxChunks && e == cudaSuccess; ++c) {
+            e = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.out[c], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "attn_fwd_host set-up");
+            return ATTN_ERR_LAUNCH;
+        }
+        hp.ready = true;
+    }
+    pipe = &hp;
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -631,6 +664,79 @@ attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k, const void *
         scratch = g_dev_scratch[dev];
     }
     return run_decode(prm, dev, D, dtype, causal, scratch, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                            void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d, int B, int Hq,
+                            int Hkv, int Nq, int Nk, int D, float scale, int causal, attn_dtype_t dtype,
+                            void *stream) {
+    gqa::Params prm;
+    int dev = 0;
+    bool empty = false;
+    attn_status_t st = prepare(q_d, k_d, v_d, o_d, lse_d, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm,
+                               dev, empty);
+    if (st != ATTN_OK || empty) return st;
+    if (!q_h || !k_h || !v_h || !o_h || (lse_h == nullptr) != (lse_d == nullptr)) return ATTN_ERR_NULL;
+
+    // Chunks of consecutive (b, kv head) groups: each group's query heads, keys,
+    // values, outputs and log-sum-exps are contiguous, so a chunk is five plain
+    // copies and one attn_fwd_kv call over B' = groups, Hq' = G, Hkv' = 1.
+    const int G = Hq / Hkv;
+    const int groups = B * Hkv;
+    const long long items = static_cast<long long>(B) * Hq * ((Nq + 255) / 256);
+    long long want = items / (2LL * g_dev_sms[dev]);  // keep every chunk's launch a full GPU or more
+    if (want > kMaxChunks) want = kMaxChunks;
+    if (want > groups) want = groups;
+    if (want < 1) want = 1;
+    const int per = static_cast<int>((groups + want - 1) / want);
+    const int chunks = (groups + per - 1) / per;
+    const size_t qb = static_cast<size_t>(G) * Nq * D * 2;  // bytes of one group's Q (and O)
+    const size_t kb = static_cast<size_t>(Nk) * D * 2;      // bytes of one group's K (and V)
+    const size_t lb = static_cast<size_t>(G) * Nq * sizeof(float);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    auto at = [](const void *base, size_t off) { return static_cast<const uint8_t *>(base) + off; };
+    auto atw = [](void *base, size_t off) { return static_cast<uint8_t *>(base) + off; };
+
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    if ((st = host_pipe(dev, hp)) != ATTN_OK) return st;
+    cudaError_t e = cudaEventRecord(hp->start, cs);  // after the caller's earlier work
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->h2d, hp->start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->start, 0);
+    for (int c = 0; c < chunks && e == cudaSuccess && st == ATTN_OK; ++c) {
+        const int g0 = c * per, ng = (groups - g0 < per) ? groups - g0 : per;
+        // copy in on h2d
+        e = cudaMemcpyAsync(atw(q_d, g0 * qb), at(q_h, g0 * qb), ng * qb, cudaMemcpyHostToDevice, hp->h2d);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(atw(k_d, g0 * kb), at(k_h, g0 * kb), ng * kb, cudaMemcpyHostToDevice, hp->h2d);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(atw(v_d, g0 * kb), at(v_h, g0 * kb), ng * kb, cudaMemcpyHostToDevice, hp->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(hp->in[c], hp->h2d);
+        // compute on the caller's stream
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, hp->in[c], 0);
+        if (e != cudaSuccess) break;
+        st = attn_fwd_kv(at(q_d, g0 * qb), at(k_d, g0 * kb), at(v_d, g0 * kb), atw(o_d, g0 * qb),
+                         lse_d ? reinterpret_cast<float *>(atw(lse_d, g0 * lb)) : nullptr, ng, G, 1, Nq, Nk, D,
+                         scale, causal, dtype, stream);
+        if (st != ATTN_OK) break;
+        e = cudaEventRecord(hp->out[c], cs);
+        // copy out on d2h
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->out[c], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(atw(o_h, g0 * qb), at(o_d, g0 * qb), ng * qb, cudaMemcpyDeviceToHost, hp->d2h);
+        if (e == cudaSuccess && lse_h)
+            e = cudaMemcpyAsync(atw(lse_h, g0 * lb), at(lse_d, g0 * lb), ng * lb, cudaMemcpyDeviceToHost,
+                                hp->d2h);
+    }
+    // the caller's stream resumes after the last copy out, also after an error above
+    cudaError_t e2 = cudaEventRecord(hp->done, hp->d2h);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(cs, hp->done, 0);
+    if (e == cudaSuccess) e = e2;
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "attn_fwd_host copies");
+        return ATTN_ERR_LAUNCH;
+    }
+    return st;
 }
 
 const char *attn_status_str(attn_status_t status) {

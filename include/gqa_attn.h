@@ -182,6 +182,35 @@ attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k, const void *
                                       float *lse, int B, int Hq, int Hkv, int Nq, int Nk, int D,
                                       float scale, int causal, attn_dtype_t dtype, void *stream);
 
+/*
+ * attn_fwd_host -- attn_fwd_kv for inputs and outputs in host memory: copies Q,
+ * K, V in, computes, copies O and LSE out, overlapping the three.
+ *
+ * The B * Hkv (batch, kv head) groups are contiguous in every tensor (a group's
+ * Hq / Hkv query heads are adjacent), so the call cuts them into up to 8 chunks
+ * of consecutive groups: chunk c + 1 is copied in on one library stream while
+ * chunk c is computed on `stream` and chunk c - 1 is copied out on another.
+ * The pages have no counterpart (their benchmarks start from device tensors).
+ *
+ * q_h, k_h, v_h       host inputs, layouts as attn_fwd_kv; page-locked memory
+ *                     makes the copies asynchronous (pageable memory works but
+ *                     serialises them)
+ * o_h, lse_h          host outputs (lse_h NULL exactly when lse_d is NULL)
+ * q_d ... lse_d       device buffers of the same sizes, owned by the caller;
+ *                     they hold the inputs and results when the call is done
+ * stream              the call is ordered after earlier work on `stream`, and
+ *                     later work on `stream` waits for its last copy out; the
+ *                     call returns without waiting.  Host outputs are valid
+ *                     once `stream` has passed that point.
+ * Set-up: the first call on a device creates the library's two copy streams
+ *   and its events (not memory; kept for the life of the process).
+ * Errors: as attn_fwd_kv; ATTN_ERR_NULL for a missing host pointer.
+ */
+attn_status_t attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h,
+                            float *lse_h, void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                            attn_dtype_t dtype, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *attn_status_str(attn_status_t status);
 

@@ -416,3 +416,55 @@ def test_decode_timeout_is_reported_and_context_survives(forced_splits):
     assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
     ro, rl = oracle_full(w, x)
     assert_parity(w, _np(o), _np(lse), ro, rl, "decode after timeout")
+
+
+# ------------------------------------------------------------------ host buffers
+def _host_call(w, x, pinned=True):
+    """attn_fwd_host on host copies of the inputs; returns (o, lse) as host tensors and
+    the device outputs."""
+    import torch
+
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+
+    def host(bits):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(dt)
+        return t.pin_memory() if pinned else t.clone()
+
+    qh, kh, vh = (host(x[n]) for n in "qkv")
+    oh = torch.empty_like(qh)
+    lh = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32)
+    if pinned:
+        oh, lh = oh.pin_memory(), lh.pin_memory()
+    qd, kd, vd = (torch.empty(t.shape, dtype=dt, device="cuda") for t in (qh, kh, vh))
+    od = torch.empty_like(qd)
+    ld = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    st = binding.attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, w.B, w.Hq, w.Hkv, w.N,
+                               w.n_keys, w.D, w.scale, w.causal, dt, s)
+    assert st == binding.ATTN_OK, binding.STATUS.get(st, st)
+    s.synchronize()
+    assert binding.attn_last_device_error(s) == binding.ATTN_OK
+    return oh, lh, od, ld
+
+
+@pytest.mark.parametrize("name", ["long_prefill_causal_gqa_bf16_n32768", "noncausal_gqa_bf16_n4096"])
+def test_host_buffers_same_bits_as_device_call(name):
+    """Chunked copies and compute give the same bits as one device-resident call
+    (each row's arithmetic does not depend on the chunking)."""
+    import torch
+
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    oh, lh, od, ld = _host_call(w, x)
+    o, lse = run_gpu(w, x)
+    assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
+    assert torch.equal(od.cpu(), oh)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffers_against_oracle(pinned):
+    w = workloads.Workload("host", 3, 8, 2, 200, 128, "bf16", True, seed=51, Nk=700)
+    x = workloads.make_inputs(w)
+    oh, lh, _, _ = _host_call(w, x, pinned=pinned)
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, oh.double().numpy(), lh.double().numpy(), ro, rl, f"host pinned={pinned}")
