@@ -468,3 +468,21 @@ def test_host_buffers_against_oracle(pinned):
     oh, lh, _, _ = _host_call(w, x, pinned=pinned)
     ro, rl = oracle_full(w, x)
     assert_parity(w, oh.double().numpy(), lh.double().numpy(), ro, rl, f"host pinned={pinned}")
+
+
+@pytest.mark.parametrize("name", ["decode_gqa_bf16_b1_q1_k32768", "decode_gqa_bf16_b16_q1_k8192",
+                                  "short_chunk_gqa_bf16_q16_k32768"])
+def test_decode_workloads_full_size(name):
+    """The benchmarked decode workloads, as bench.py runs them (attn_fwd_decode with the
+    workspace it asks for): every row against the oracle."""
+    import torch
+
+    w = workloads.WORKLOADS[name]
+    assert w.entry == "attn_fwd_decode"
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o, lse = binding.attention_decode(q, k, v, causal=w.causal, scale=w.scale)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    err = assert_parity(w, _np(o), _np(lse), ro, rl, name)
+    print(f"{name}: max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
