@@ -414,7 +414,7 @@ def run_ours(args):
                        "host_us_per_call": None if host_us is None else round(host_us, 2)},
             "clocks": clock_info,
         }
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:  # rank 0 at N = 1 only
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if world > 1:
