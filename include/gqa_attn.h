@@ -11,7 +11,9 @@
  *     hq / (Hq / Hkv) of the same batch entry (same section's kernel: the
  *     flattened (b, q_head) index divided by the group count);
  *   - the optional causal mask j <= i on absolute row indices (same section:
- *     positions with offsets_qm >= offsets_kk are kept);
+ *     positions with offsets_qm >= offsets_kk are kept); with Nq query rows
+ *     over Nk keys (attn_fwd_kv and the calls built on it) the query rows are
+ *     the last Nq positions, so row i keeps keys j <= i + Nk - Nq;
  *   - the natural-log log-sum-exp of each masked, scaled score row,
  *     lse = max_j s_ij + ln(sum_j exp(s_ij - max_j s_ij)), written as fp32.
  *
@@ -252,8 +254,9 @@ void attn_test_inject_stall(int enable);
  */
 void attn_test_select_kernel(int which);
 
-/* attn_test_force_splits: n > 0 makes attn_fwd_decode use n key splits (as far
- * as the key tiles and the workspace allow); 0 restores its own choice. */
+/* attn_test_force_splits: n > 0 makes attn_fwd_decode and attn_fwd_decode_noalloc
+ * use n key splits (as far as the key tiles and the workspace allow); 0 restores
+ * their own choice. */
 void attn_test_force_splits(int n_splits);
 
 #ifdef __cplusplus
