@@ -190,11 +190,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
-# the files the persistent prefill kernel (attn_fwd_ws_kernel) is compiled from
+# the files that hold the persistent prefill kernel's code (attn_fwd_ws_kernel)
 KERNEL_SOURCES = ("gqa_attention_forward_gb300/csrc/attn_fwd_ws.cuh",
                   "gqa_attention_forward_gb300/csrc/kernel_common.cuh",
-                  "gqa_attention_forward_gb300/csrc/sm103_ptx.cuh",
-                  "include/gqa_attn.h")
+                  "gqa_attention_forward_gb300/csrc/sm103_ptx.cuh")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_ws_long_prefill_full.md")
 
 
