@@ -629,12 +629,12 @@ attn_status_t attn_fwd_decode_workspace(int B, int Hq, int Hkv, int Nq, int Nk, 
 attn_status_t attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                               int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
                               attn_dtype_t dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_ERR_ALIGN;
     gqa::Params prm;
     int dev = 0;
     bool empty = false;
     attn_status_t st = prepare(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm, dev, empty);
     if (st != ATTN_OK || empty) return st;
-    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_ERR_ALIGN;
     const long long cap = workspace == nullptr ? 1 : static_cast<long long>(workspace_bytes / split_bytes(prm, D));
     plan_splits(prm, g_dev_sms[dev], cap);
     return run_decode(prm, dev, D, dtype, causal, workspace, static_cast<cudaStream_t>(stream));
@@ -670,13 +670,15 @@ attn_status_t attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, v
                             void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d, int B, int Hq,
                             int Hkv, int Nq, int Nk, int D, float scale, int causal, attn_dtype_t dtype,
                             void *stream) {
+    const bool non_empty = B > 0 && Hq > 0 && Nq > 0;
+    if (non_empty && (!q_h || !k_h || !v_h || !o_h || (lse_h == nullptr) != (lse_d == nullptr)))
+        return ATTN_ERR_NULL;
     gqa::Params prm;
     int dev = 0;
     bool empty = false;
     attn_status_t st = prepare(q_d, k_d, v_d, o_d, lse_d, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm,
                                dev, empty);
     if (st != ATTN_OK || empty) return st;
-    if (!q_h || !k_h || !v_h || !o_h || (lse_h == nullptr) != (lse_d == nullptr)) return ATTN_ERR_NULL;
 
     // Chunks of consecutive (b, kv head) groups: each group's query heads, keys,
     // values, outputs and log-sum-exps are contiguous, so a chunk is five plain

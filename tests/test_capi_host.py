@@ -131,3 +131,47 @@ def test_kv_empty_and_non_causal_longer_queries(lib):
     # Nq > Nk is fine without the mask, and Nq == Nk is attn_fwd: both pass validation
     assert _kv(lib, Nq=64, Nk=48, causal=0) == 8
     assert _kv(lib, Nq=48, Nk=48) == 8
+
+
+def test_decode_and_host_entry_points_validate_first(lib):
+    """attn_fwd_decode, attn_fwd_decode_noalloc, attn_fwd_host and the workspace query
+    reject bad arguments before touching a device; valid ones reach the device check."""
+    torch = pytest.importorskip("torch")
+    dims = dict(B=1, Hq=8, Hkv=2, Nq=3, Nk=500, D=128)
+
+    def dec(**o):
+        a = dict(dims, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, causal=1, ws=None, nbytes=0)
+        a.update(o)
+        return binding.attn_fwd_decode(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"],
+                                       a["Hkv"], a["Nq"], a["Nk"], a["D"], 0.1, a["causal"], 1,
+                                       a["ws"], a["nbytes"], None)
+
+    def noalloc(**o):
+        a = dict(dims, q=FAKE, causal=1)
+        a.update(o)
+        return binding.attn_fwd_decode_noalloc(a["q"], FAKE, FAKE, FAKE, None, a["B"], a["Hq"],
+                                               a["Hkv"], a["Nq"], a["Nk"], a["D"], 0.1,
+                                               a["causal"], 1, None)
+
+    def host(**o):
+        a = dict(dims, qh=FAKE, oh=FAKE, lh=None, ld=None)
+        a.update(o)
+        return binding.attn_fwd_host(a["qh"], FAKE, FAKE, a["oh"], a["lh"], FAKE, FAKE, FAKE, FAKE,
+                                     a["ld"], a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["D"],
+                                     0.1, 1, 1, None)
+
+    assert dec(Nq=600) == 2            # causal with Nq > Nk
+    assert dec(D=96) == 3
+    assert dec(q=0) == 1
+    assert dec(ws=FAKE + 8, nbytes=1 << 20) == 5   # misaligned workspace
+    assert dec(B=0, q=None) == 0       # empty problem
+    assert noalloc(Hq=6, Hkv=4) == 2
+    assert noalloc(q=FAKE + 2) == 5
+    assert host(qh=None) == 1          # missing host input
+    assert host(lh=FAKE) == 1          # lse_h without lse_d
+    assert host(Nk=0) == 2
+    st, nbytes = binding.attn_fwd_decode_workspace(1, 8, 3, 1, 100, 128)
+    assert st == 2 and nbytes == 0     # Hq % Hkv != 0
+    if not torch.cuda.is_available():
+        assert dec() == 8 and noalloc() == 8 and host() == 8
+        assert binding.attn_fwd_decode_workspace(1, 8, 2, 1, 100, 128)[0] == 8
