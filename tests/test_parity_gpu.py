@@ -486,3 +486,42 @@ def test_decode_workloads_full_size(name):
     ro, rl = oracle_full(w, x)
     err = assert_parity(w, _np(o), _np(lse), ro, rl, name)
     print(f"{name}: max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
+
+
+# ------------------------------------------------------------------ randomized sweep
+def _random_problems(count=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for t in range(count):
+        B = int(rng.integers(1, 4))
+        Hkv = int(rng.choice([1, 2, 4]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        causal = bool(rng.integers(0, 2))
+        Nq = int(rng.integers(1, 300))
+        Nk = int(rng.integers(Nq, 1500)) if causal else int(rng.integers(1, 1500))
+        D = int(rng.choice([64, 128]))
+        dtype = str(rng.choice(["f16", "bf16"]))
+        std = float(rng.choice([1.0, 3.0]))
+        out.append((t, B, G * Hkv, Hkv, Nq, Nk, D, dtype, causal, std))
+    return out
+
+
+@pytest.mark.parametrize("prob", _random_problems(), ids=lambda p: "x".join(map(str, p)))
+def test_random_problems_all_entry_points(prob):
+    """Seeded random problems through attn_fwd_kv, attn_fwd_decode and attn_fwd_host,
+    each against the oracle."""
+    import torch
+
+    t, B, Hq, Hkv, Nq, Nk, D, dtype, causal, std = prob
+    w = workloads.Workload("fuzz", B, Hq, Hkv, Nq, D, dtype, causal, q_std=std, k_std=std,
+                           seed=3000 + t, Nk=Nk)
+    x = workloads.make_inputs(w)
+    ro, rl = oracle_full(w, x)
+    q, k, v = (to_device(x[n], dtype) for n in "qkv")
+    o1, l1 = binding.attention(q, k, v, causal=causal, scale=w.scale)
+    o2, l2 = binding.attention_decode(q, k, v, causal=causal, scale=w.scale)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    assert_parity(w, _np(o1), _np(l1), ro, rl, f"{prob} attn_fwd_kv")
+    assert_parity(w, _np(o2), _np(l2), ro, rl, f"{prob} attn_fwd_decode")
+    oh, lh, _, _ = _host_call(w, x)
+    assert_parity(w, oh.double().numpy(), lh.double().numpy(), ro, rl, f"{prob} attn_fwd_host")
