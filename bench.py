@@ -444,7 +444,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded i.i.d. normal)", "impl": "reference",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
-                       "D": w.D, "causal": w.causal},
+                       "Nk": w.n_keys, "D": w.D, "causal": w.causal},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": s.threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,

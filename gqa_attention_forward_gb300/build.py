@@ -10,7 +10,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgqa_attn.so")
 SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]
-HEADERS = ["sm103_ptx.cuh", "kernel_common.cuh", "attn_fwd_ws.cuh"]
+# every header under csrc/ (and the public one) is a dependency of the library
+HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
 DEPENDS = SOURCES + [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "gqa_attn.h")]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]

@@ -649,9 +649,13 @@ attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k, const void *
     attn_status_t st = prepare(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm, dev, empty);
     if (st != ATTN_OK || empty) return st;
     plan_splits(prm, g_dev_sms[dev], LLONG_MAX);
+    if (prm.n_splits > 1 && split_bytes(prm, D) * prm.n_splits > ATTN_NOALLOC_SCRATCH_BYTES)
+        return ATTN_ERR_SCRATCH;
+    // Every call that gets this far looks the buffer up on its first use on the
+    // device, whether or not this plan splits, so that any one successful call
+    // made before a stream capture has done the (non-stream) lookup.
     void *scratch = nullptr;
-    if (prm.n_splits > 1) {
-        if (split_bytes(prm, D) * prm.n_splits > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH;
+    {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         if (g_dev_scratch[dev] == nullptr) {
             cudaError_t e = cudaGetSymbolAddress(&g_dev_scratch[dev], g_noalloc_scratch);
@@ -663,7 +667,8 @@ attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k, const void *
         }
         scratch = g_dev_scratch[dev];
     }
-    return run_decode(prm, dev, D, dtype, causal, scratch, static_cast<cudaStream_t>(stream));
+    return run_decode(prm, dev, D, dtype, causal, prm.n_splits > 1 ? scratch : nullptr,
+                      static_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,

@@ -422,6 +422,19 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const Params p) {
     const long long R = static_cast<long long>(blockIdx.x) * 4 + warp;
     if (R >= p.total_rows) return;
     constexpr int kPer = D / 32;
+    if (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) {
+        // The split kernel of this call gave up on a wait, so some pieces were
+        // never written (with a shared buffer they would be an earlier call's):
+        // mark the row as undefined instead of merging stale partials.
+        uint8_t *dst = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(R) * D + lane * kPer) * 2;
+        const uint32_t nan2 = kBF16 ? 0x7FC07FC0u : 0x7E007E00u;
+        if constexpr (kPer == 4)
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(nan2, nan2);
+        else
+            *reinterpret_cast<uint32_t *>(dst) = nan2;
+        if (p.lse != nullptr && lane == 0) p.lse[R] = __int_as_float(0x7FC00000);
+        return;
+    }
     constexpr int kBatch = 16;  // pieces whose loads are in flight together
     const int S = p.n_splits;
     const size_t stride = static_cast<size_t>(p.total_rows);

@@ -40,6 +40,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Arrive once on `bar` and raise its expected transaction count by `bytes`
+// (the bytes that asynchronous copies will deliver to it).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+// Tiled tensor copy of one box from global memory into shared memory; its
+// bytes complete a transaction on `bar`.  The operands are taken in the order
+// the instruction lists them: destination, tensor map with the coordinates
+// {x, y, z} (x innermost, in elements; x * element size must be a multiple of
+// 16 bytes), then the mbarrier.  `map` is the generic address of a
+// __grid_constant__ kernel parameter.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const void *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy that bypasses L1; src_bytes < 16 zero-fills
 // the rest of the 16 bytes (0 reads nothing).

@@ -169,8 +169,9 @@ attn_status_t attn_fwd_decode_workspace(int B, int Hq, int Hkv, int Nq, int Nk, 
  * before anything is launched.
  *
  * Arguments, layout, masks and errors: as attn_fwd_kv.
- * Setup: the first call on a device looks up the buffer's address (not a
- *   stream operation); make one call on each device before capturing calls
+ * Setup: the first call on a device that passes argument validation looks
+ *   up the buffer's address (not a stream operation), whether or not its plan
+ *   splits the keys; make one such call on each device before capturing calls
  *   into a CUDA graph.
  * Contents: nothing in the buffer needs to start at any value; each call
  *   writes every part it reads.

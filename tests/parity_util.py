@@ -2,6 +2,9 @@
 run the float64 oracle on the same seeded inputs, and compare."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 import oracle
@@ -50,6 +53,36 @@ def errors(o_gpu: np.ndarray, lse_gpu, o_ref: np.ndarray, lse_ref):
     if lse_gpu is not None and lse_ref.size:
         err_lse = float(np.max(np.abs(lse_gpu - lse_ref) / np.maximum(1.0, np.abs(lse_ref))))
     return err_o, err_lse
+
+
+# Significand bits after the leading one: the spacing of representable values
+# in [2^e, 2^(e+1)) is 2^(e - bits); below the smallest normal the spacing stays
+# that of the smallest normal binade.
+_FRAC_BITS = {"bf16": 7, "f16": 10}
+_MIN_EXP = {"bf16": -126, "f16": -14}
+
+
+def ulp_of(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Spacing of the 16-bit storage type's values at |x| (one unit in the last place)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, np.finfo(np.float64).tiny)))
+    e = np.maximum(e, _MIN_EXP[dtype])
+    return np.exp2(e - _FRAC_BITS[dtype])
+
+
+def ulp_error(o_gpu: np.ndarray, o_ref: np.ndarray, dtype: str) -> float:
+    """max over elements of |O_gpu - O_ref| in units of the storage type's ulp at |O_ref|."""
+    if o_ref.size == 0:
+        return 0.0
+    return float(np.max(np.abs(o_gpu - o_ref) / ulp_of(o_ref, dtype)))
+
+
+def record(entry: dict) -> None:
+    """Append one parity result to the JSON-lines file named by GQA_PARITY_LOG, if set."""
+    path = os.environ.get("GQA_PARITY_LOG")
+    if path:
+        with open(path, "a") as fh:
+            fh.write(json.dumps(entry) + "\n")
 
 
 def assert_parity(w, o_gpu, lse_gpu, o_ref, lse_ref, what=""):
