@@ -9,9 +9,14 @@ resident in HBM.  Prints one JSON line (rank 0):
   e2e        the same metric with host->device input copies and the
              device->host read of O and LSE inside the timed region;
   cpu_baseline  the float64 oracle timed on the host cores on a row sample.
+``--all`` prints that line first and then one line for each of the other
+benchmarked workloads (the short and L2-resident ones timed both with L2
+flushed between launches, which gives ``value``, and warm).
 ``--impl reference`` times the float64 oracle alone (CPU) on the same metric.
-Under torchrun each rank runs its own replica of the workload on its own GPU
-(weak scaling, no collective on the data path).
+Under torchrun the (batch, kv head) groups of the problem are split into
+contiguous ranges, one per rank, with no collective on the data path: by
+default the job is a batch of one workload per rank (weak scaling);
+``--partition strong`` splits the groups of one workload instead.
 """
 from __future__ import annotations
 
@@ -52,7 +57,58 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph holding one step (launch-overhead path)")
+    ap.add_argument("--all", action="store_true",
+                    help="after the headline line, one line for each workload in ALL_WORKLOADS")
+    ap.add_argument("--partition", choices=["weak", "strong"], default="weak",
+                    help="weak: each rank takes the groups of its own batch entries of a batch "
+                         "that grows with the ranks; strong: the ranks split one workload")
+    ap.add_argument("--item-order", type=int, choices=[0, 1], default=None,
+                    help="work-item order of the persistent kernel (library default if unset)")
     return ap.parse_args()
+
+
+# the headline workload first, then the other configurations and next-step workloads
+ALL_WORKLOADS = [DEFAULT_WORKLOAD, "tiny_causal_gqa_f16", "pages_shape_causal_gqa_f16",
+                 "noncausal_gqa_bf16_n4096", "tail_stress_causal_gqa_bf16_n2000",
+                 "chunked_prefill_causal_gqa_bf16_q4096_k32768", "decode_gqa_bf16_b1_q1_k32768",
+                 "decode_gqa_bf16_b16_q1_k8192", "short_chunk_gqa_bf16_q16_k32768"]
+L2_BYTES = 126 * 2 ** 20  # GB300 L2 (129 MB as the device reports it)
+FLUSH_BYTES = 256 * 2 ** 20
+
+
+def group_range(total: int, world: int, rank: int):
+    """Contiguous range [g0, g1) of `total` (batch, kv head) groups owned by `rank`:
+    the ranges of ranks 0..world-1 cover every group exactly once, in order, and
+    differ in size by at most one."""
+    base, extra = divmod(total, world)
+    g0 = rank * base + min(rank, extra)
+    return g0, g0 + base + (1 if rank < extra else 0)
+
+
+def slice_groups(w, x: dict, g0: int, g1: int) -> dict:
+    """The inputs of groups [g0, g1) of workload w: a (b, kv head) group's G query
+    heads, its keys and its values are contiguous in [B, H, N, D], so a group range
+    is a plain slice of each tensor, laid out as a problem with B = g1 - g0, Hq = G
+    and Hkv = 1."""
+    G = w.Hq // w.Hkv
+    return {"q": x["q"].reshape(w.B * w.Hkv, G, w.N, w.D)[g0:g1],
+            "k": x["k"].reshape(w.B * w.Hkv, 1, w.n_keys, w.D)[g0:g1],
+            "v": x["v"].reshape(w.B * w.Hkv, 1, w.n_keys, w.D)[g0:g1]}
+
+
+def rank_problem(w, partition: str, world: int, rank: int):
+    """(sub-workload, inputs, global FLOPs per step) of this rank.
+
+    weak: the job is a batch of `world` copies of w; rank r's groups are those of
+    its own copy, drawn from seed w.seed + r.  strong: the job is w itself; rank r
+    takes group_range(B*Hkv, world, r) of it (possibly none)."""
+    if partition == "weak" or world == 1:
+        seed = w.seed + rank
+        return w, workloads.make_inputs(w, seed=seed), w.flops * world
+    total = w.B * w.Hkv
+    g0, g1 = group_range(total, world, rank)
+    sub = w.with_(name=w.name, B=g1 - g0, Hq=w.Hq // w.Hkv, Hkv=1)
+    return sub, slice_groups(w, workloads.make_inputs(w), g0, g1), w.flops
 
 
 def dist_env():
@@ -194,7 +250,7 @@ class ClockSampler:
 KERNEL_SOURCES = ("gqa_attention_forward_gb300/csrc/attn_fwd_ws.cuh",
                   "gqa_attention_forward_gb300/csrc/kernel_common.cuh",
                   "gqa_attention_forward_gb300/csrc/sm103_ptx.cuh")
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_ws_long_prefill_full.md")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
 def kernel_source_digest() -> str:
@@ -211,18 +267,28 @@ def kernel_source_digest() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    this workload with the current kernel sources; otherwise None."""
+    """DRAM bytes per launch of the persistent kernel from a committed ncu summary
+    (any file under profiles/ whose 'workload:' line names this workload), if it
+    was taken with the current kernel sources; otherwise None."""
     try:
-        with open(TRAFFIC_PROFILE) as fh:
-            kv = dict(line.split(": ", 1) for line in fh.read().splitlines() if ": " in line)
+        names = sorted(os.listdir(PROFILES))
     except OSError:
         return None
-    if kv.get("workload", "").strip() != workload:
-        return None
-    if kv.get("kernel_source_sha256", "").strip() != kernel_source_digest():
-        return None
-    return int(kv["dram_bytes_per_launch"])
+    digest = None
+    for name in names:
+        if not name.endswith(".md"):
+            continue
+        try:
+            with open(os.path.join(PROFILES, name)) as fh:
+                kv = dict(line.split(": ", 1) for line in fh.read().splitlines() if ": " in line)
+        except OSError:
+            continue
+        if kv.get("workload", "").strip() != workload or "dram_bytes_per_launch" not in kv:
+            continue
+        digest = digest or kernel_source_digest()
+        if kv.get("kernel_source_sha256", "").strip() == digest:
+            return int(kv["dram_bytes_per_launch"])
+    return None
 
 
 def to_dev(bits, dtype, device):
@@ -232,19 +298,21 @@ def to_dev(bits, dtype, device):
     return t.view(torch.float16 if dtype == "f16" else torch.bfloat16).to(device)
 
 
-def run_ours(args):
+def algorithmic_bytes(w) -> int:
+    """Q, K, V read once, O written once, LSE written once."""
+    return 2 * w.B * w.D * (2 * w.Hq * w.N + 2 * w.Hkv * w.n_keys) + 4 * w.B * w.Hq * w.N
+
+
+def measure(w_full, args, rank, world, device):
+    """Times one workload on this rank; returns rank 0's JSON line (None elsewhere)."""
     import torch
     import torch.distributed as dist
 
     from gqa_attention_forward_gb300 import binding
 
-    rank, world, local = dist_env()
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    device = torch.device("cuda", torch.cuda.current_device())
-    w = workloads.WORKLOADS[args.workload]
-    x = workloads.make_inputs(w, seed=w.seed + rank)  # each rank: its own replica
+    w, x, job_flops = rank_problem(w_full, args.partition, world, rank)
+    has_work = w.B > 0
+    flops_rank = w.flops if has_work else 0.0
     q, k, v = (to_dev(x[n], w.dtype, device) for n in "qkv")
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=device)
@@ -253,13 +321,15 @@ def run_ours(args):
     square = w.n_keys == w.N
     decode = w.entry == "attn_fwd_decode"
     workspace, ws_bytes = None, 0
-    if decode:
+    if decode and has_work:
         st, ws_bytes = binding.attn_fwd_decode_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D)
         if st != binding.ATTN_OK:
             raise binding.AttnError(st, "attn_fwd_decode_workspace")
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
 
     def launch():
+        if not has_work:
+            return
         s_now = torch.cuda.current_stream(device)  # the capture stream while capturing
         if decode:
             st = binding.attn_fwd_decode(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
@@ -277,7 +347,7 @@ def run_ours(args):
     host_us = None
     launch()  # the first call of a variant configures the kernel (and, in graph mode,
     torch.cuda.synchronize()  # must come before the capture)
-    if args.graph:
+    if args.graph and has_work:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             launch()
@@ -285,7 +355,7 @@ def run_ours(args):
 
     for _ in range(max(args.warmup, 3)):
         step()
-    if not args.graph:
+    if not args.graph and has_work:
         # host cost of one call through the Python binding (validation + launch), on
         # warm calls queued back to back
         torch.cuda.synchronize()
@@ -298,34 +368,51 @@ def run_ours(args):
     if st != binding.ATTN_OK:
         raise binding.AttnError(st, "warm-up")
 
-    # ---- device-resident timing: K launches, one event pair per launch
+    # Inputs and outputs that fit in L2 would stay there between launches: such a
+    # workload is timed with L2 flushed before every launch (a 256 MB write outside
+    # the timed events), which gives `value`, and warm as well.
+    in_l2 = 2 * w_full.B * w_full.D * (w_full.Hq * w_full.N + 2 * w_full.Hkv * w_full.n_keys) <= L2_BYTES
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if in_l2 else None
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    clocks = ClockSampler(device.index if world == 1 else local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    for i in range(K):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    clock_info = clocks.stop()
-    if world > 1:
-        dist.barrier()
-    st = binding.attn_last_device_error(stream)
-    if st != binding.ATTN_OK:
-        raise binding.AttnError(st, "timed region")
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = starts[0].elapsed_time(ends[-1])
-    total_ms = max_over_ranks(total_ms, device)
-    value = whole_job_tflops(w.flops, K, world, total_ms)
-    kern_ms = float(np.mean(per_launch_ms))
-    achieved = w.flops / (kern_ms / 1e3) / 1e12
 
-    # ---- end to end: pinned host inputs -> device -> attn_fwd -> O, LSE back to host
+    def timed(flushed: bool):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(device.index if world == 1 else int(os.environ.get("LOCAL_RANK", 0)))
+        clocks.start()
+        for i in range(K):
+            if flushed:
+                flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        clock_info = clocks.stop()
+        if world > 1:
+            dist.barrier()
+        st = binding.attn_last_device_error(stream)
+        if st != binding.ATTN_OK:
+            raise binding.AttnError(st, "timed region")
+        per_launch = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        # back to back: first start to last end; flushed: the launches alone
+        span = starts[0].elapsed_time(ends[-1]) if not flushed else float(np.sum(per_launch))
+        return max_over_ranks(span, device), float(np.mean(per_launch)), clock_info
+
+    warm = None
+    if in_l2:
+        warm_ms, warm_kern, _ = timed(False)
+        warm = {"ms_per_step": round(warm_ms / K, 5),
+                "value": round(job_flops * K / (warm_ms / 1e3) / 1e12, 2)}
+        total_ms, kern_ms, clock_info = timed(True)
+    else:
+        total_ms, kern_ms, clock_info = timed(False)
+    value = job_flops * K / (total_ms / 1e3) / 1e12
+    achieved = flops_rank / (kern_ms / 1e3) / 1e12 if has_work else 0.0
+
+    # ---- end to end: pinned host inputs -> device -> attention -> O, LSE back to host
     hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(x[n]).view(np.int16)).pin_memory()
                   for n in "qkv")
     ho = torch.empty(o.numel(), dtype=torch.int16).pin_memory()
@@ -335,6 +422,8 @@ def run_ours(args):
     E = max(1, min(args.e2e_steps, K))
 
     def e2e_step():
+        if not has_work:
+            return
         if decode:
             dq.copy_(hq.view(-1), non_blocking=True)
             dk.copy_(hk.view(-1), non_blocking=True)
@@ -351,71 +440,105 @@ def run_ours(args):
 
     e2e_step()  # first call creates the library's copy streams
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / E
-    e2e_ms = max_over_ranks(e2e_ms, device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, device)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * 2 + hl.numel() * 4
+    if rank != 0:
+        return None
 
-    if rank == 0:
-        # Q, K, V read once, O written once, LSE written once
-        algo_bytes = (2 * w.B * w.D * (2 * w.Hq * w.N + 2 * w.Hkv * w.n_keys)
-                      + 4 * w.B * w.Hq * w.N)
-        peaks, peak_src = load_peaks()
-        long_region = total_ms > 1000.0
-        if decode:
-            # streams K and V once: bound by HBM bandwidth, not the tensor core
-            gbs = algo_bytes / (kern_ms / 1e3) / 1e9
-            roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                        "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                        "traffic": profiled_traffic(w.name), "algorithmic_bytes": algo_bytes,
-                        "peak_source": f"{peak_src} copy bandwidth",
-                        "kernel": "gqa::attn_fwd_decode_kernel"
-                                  + (" + gqa::attn_combine_kernel" if ws_bytes else ""),
-                        "kernel_ms": round(kern_ms, 4), "tflops": round(achieved, 2)}
-        else:
-            peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
-            roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                        "unit": UNIT, "frac": round(achieved / peak, 4),
-                        "traffic": profiled_traffic(w.name), "algorithmic_bytes": algo_bytes,
-                        "peak_source": f"{peak_src} "
-                                       f"{'sustained' if long_region else 'burst'} bf16",
-                        "kernel": "gqa::attn_fwd_ws_kernel", "kernel_ms": round(kern_ms, 4),
-                        "frac_of_2250_nominal": round(achieved / 2250.0, 4)}
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-            "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms / K, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic (seeded i.i.d. normal, see workloads.py)",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
-                       "Nk": w.n_keys, "D": w.D, "causal": w.causal,
-                       "flops_per_step": w.flops,
-                       "flop_convention": "2*B*Hq*N^2*D causal, 4*B*Hq*N^2*D non-causal "
-                                          "(N query rows over Nk keys: 4*B*Hq*D*(N*Nk - N^2/2) "
-                                          "causal, 4*B*Hq*D*N*Nk non-causal)",
-                       "l2": "inputs larger than L2 (no flush)" if
-                             (2 * w.B * w.D * (w.Hq * w.N + 2 * w.Hkv * w.n_keys)) > 129e6 else
-                             "inputs smaller than L2 (not flushed)",
-                       "parallelism": f"replica x{world}"},
-            "roofline": roofline,
-            "e2e": {"value": round(whole_job_tflops(w.flops, 1, world, e2e_ms), 2), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": round(e2e_ms, 4),
-                    "path": ("torch copies around attn_fwd_decode" if decode else
-                             "attn_fwd_host: pinned host buffers, chunked copies overlapping compute")},
-            "gpu_launches": K * (2 if ws_bytes else 1),
-            "launch": {"mode": "cuda_graph_replay" if args.graph else "direct",
-                       "host_us_per_call": None if host_us is None else round(host_us, 2)},
-            "clocks": clock_info,
-        }
-        if not args.no_cpu_baseline and world == 1:  # rank 0 at N = 1 only
-            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
-        print(json.dumps(line), flush=True)
+    algo_bytes = algorithmic_bytes(w)
+    peaks, peak_src = load_peaks()
+    long_region = total_ms > 1000.0
+    gbs = algo_bytes / (kern_ms / 1e3) / 1e9 if has_work else 0.0
+    if decode:
+        # streams K and V once: bound by HBM bandwidth, not the tensor core
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                    "traffic": profiled_traffic(w_full.name), "algorithmic_bytes": algo_bytes,
+                    "peak_source": f"{peak_src} copy bandwidth",
+                    "kernel": "gqa::attn_fwd_decode_kernel"
+                              + (" + gqa::attn_combine_kernel" if ws_bytes else ""),
+                    "kernel_ms": round(kern_ms, 5), "tflops": round(achieved, 2)}
+    else:
+        peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                    "unit": UNIT, "frac": round(achieved / peak, 4),
+                    "traffic": profiled_traffic(w_full.name), "algorithmic_bytes": algo_bytes,
+                    "peak_source": f"{peak_src} {'sustained' if long_region else 'burst'} bf16",
+                    "kernel": "gqa::attn_fwd_ws_kernel", "kernel_ms": round(kern_ms, 5),
+                    "frac_of_2250_nominal": round(achieved / 2250.0, 4),
+                    # the algorithmic bytes over the same launch time, against the copy bandwidth
+                    "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+    if args.partition == "strong" and world > 1:
+        parallelism = f"groups of one problem split over {world} ranks"
+    else:
+        parallelism = f"batch of {world} x the workload, (b, kv head) groups split by rank"
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "strong" if (args.partition == "strong" and world > 1) else "weak",
+        "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded i.i.d. normal, see workloads.py)",
+        "config": {"workload": w_full.name, "B": w_full.B, "Hq": w_full.Hq, "Hkv": w_full.Hkv,
+                   "N": w_full.N, "Nk": w_full.n_keys, "D": w_full.D, "causal": w_full.causal,
+                   "flops_per_step": job_flops,
+                   "flop_convention": "2*B*Hq*N^2*D causal, 4*B*Hq*N^2*D non-causal "
+                                      "(N query rows over Nk keys: 4*B*Hq*D*(N*Nk - N^2/2) "
+                                      "causal, 4*B*Hq*D*N*Nk non-causal)",
+                   "l2": ("inputs fit in L2: flushed (256 MB write) before every timed launch"
+                          if in_l2 else "inputs larger than L2 (no flush)"),
+                   "parallelism": parallelism},
+        "roofline": roofline,
+        "e2e": {"value": round(job_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4),
+                "path": ("torch copies around attn_fwd_decode" if decode else
+                         "attn_fwd_host: pinned host buffers, chunked copies overlapping compute")},
+        "gpu_launches": K * (2 if ws_bytes else 1) * (1 if has_work else 0),
+        "launch": {"mode": "cuda_graph_replay" if args.graph else "direct",
+                   "host_us_per_call": None if host_us is None else round(host_us, 2)},
+        "clocks": clock_info,
+    }
+    if warm is not None:
+        line["l2_warm"] = warm
+    return line
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from gqa_attention_forward_gb300 import binding
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    if args.item_order is not None:
+        binding.load().attn_test_set_item_order(args.item_order)
+    names = ALL_WORKLOADS if args.all else [args.workload]
+    if args.all and args.workload != DEFAULT_WORKLOAD:
+        names = [args.workload] + [n for n in ALL_WORKLOADS if n != args.workload]
+    for i, name in enumerate(names):
+        w = workloads.WORKLOADS[name]
+        line = measure(w, args, rank, world, device)
+        if rank == 0:
+            if not args.no_cpu_baseline and world == 1:  # rank 0 at N = 1 only
+                secs = args.cpu_seconds if i == 0 else min(args.cpu_seconds, 5.0)
+                line["cpu_baseline"] = cpu_baseline(w, secs)
+            print(json.dumps(line), flush=True)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

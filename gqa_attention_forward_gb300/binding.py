@@ -72,6 +72,8 @@ def load(path: str | None = None):
         lib.attn_test_inject_stall.restype = None
         lib.attn_test_select_kernel.argtypes = [i]
         lib.attn_test_select_kernel.restype = None
+        lib.attn_test_set_item_order.argtypes = [i]
+        lib.attn_test_set_item_order.restype = None
         if path is None:
             _lib = lib
         return lib

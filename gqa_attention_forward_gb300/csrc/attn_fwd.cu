@@ -361,6 +361,40 @@ struct HostPipe {
 std::mutex g_pipe_mu;  // serialises the enqueueing of attn_fwd_host calls
 HostPipe g_pipe[kMaxDevices];
 std::atomic<int> g_kernel_choice{0};   // 0 persistent warp-specialised, 1 one CTA per query tile
+std::atomic<int> g_item_order{0};      // work-item order of the persistent kernel (0 or 1)
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map of a [heads, rows, D] array of 2-byte elements viewed as the 3-D
+// tensor (D, rows, heads): a box of 64 columns x 128 rows x 1 head lands in
+// shared memory in the 128-byte swizzle, and rows past `rows` read as zeros,
+// so a box never reaches into the next head.
+bool encode_rows_map(CUtensorMap *map, const void *base, bool bf16, int D, int rows, long long heads) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(heads)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 attn_status_t check_device(int *dev_out) {
     int dev = 0;
@@ -405,20 +439,29 @@ attn_status_t set_smem_limit(int dev, int kid, K kern, int smem) {
 
 template <int D, bool BF16, bool CAUSAL>
 attn_status_t launch(int dev, int kid, const gqa::Params &prm, cudaStream_t stream) {
-    const bool persistent = g_kernel_choice.load() == 0;
-    auto kern = persistent ? gqa::attn_fwd_ws_kernel<D, BF16, CAUSAL> : gqa::attn_fwd_kernel<D, BF16, CAUSAL>;
-    const int smem = persistent ? gqa::WsLayout<D>::kAlloc : gqa::Layout<D>::kAlloc;
-    const int threads = persistent ? gqa::kWsThreads : gqa::kThreads;
-    if (persistent) kid += 8;
-    unsigned grid;
-    if (persistent) {
+    if (g_kernel_choice.load() == 0) {
+        // persistent kernel: one CTA per SM (or per item when there are fewer), TMA loads
+        auto kern = gqa::attn_fwd_ws_kernel<D, BF16, CAUSAL>;
+        constexpr int smem = gqa::WsLayout<D>::kAlloc;
+        if (attn_status_t st = set_smem_limit(dev, kid + 8, kern, smem); st != ATTN_OK) return st;
+        CUtensorMap tq, tk, tv;
+        const long long BHkv = prm.BHq / prm.group;
+        if (!encode_rows_map(&tq, prm.q, BF16, D, prm.Nq, prm.BHq) ||
+            !encode_rows_map(&tk, prm.k, BF16, D, prm.Nk, BHkv) ||
+            !encode_rows_map(&tv, prm.v, BF16, D, prm.Nk, BHkv)) {
+            std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
+            return ATTN_ERR_LAUNCH;
+        }
         const int sms = g_dev_sms[dev];
-        grid = static_cast<unsigned>(prm.n_items < sms ? prm.n_items : sms);
+        const unsigned grid = static_cast<unsigned>(prm.n_items < sms ? prm.n_items : sms);
+        kern<<<grid, gqa::kWsThreads, smem, stream>>>(tq, tk, tv, prm);
     } else {
-        grid = static_cast<unsigned>(static_cast<long long>(prm.BHq) * prm.n_qtiles);
+        auto kern = gqa::attn_fwd_kernel<D, BF16, CAUSAL>;
+        constexpr int smem = gqa::Layout<D>::kAlloc;
+        if (attn_status_t st = set_smem_limit(dev, kid, kern, smem); st != ATTN_OK) return st;
+        const unsigned grid = static_cast<unsigned>(static_cast<long long>(prm.BHq) * prm.n_qtiles);
+        kern<<<grid, gqa::kThreads, smem, stream>>>(prm);
     }
-    if (attn_status_t st = set_smem_limit(dev, kid, kern, smem); st != ATTN_OK) return st;
-    kern<<<grid, threads, smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         note_cuda_error(e, "kernel launch");
@@ -508,6 +551,7 @@ attn_status_t prepare(const void *q, const void *k, const void *v, void *o, floa
     prm.seq = g_launch_seq.fetch_add(1);
     prm.timeout_ns = g_timeout_ns.load();
     prm.inject_stall = g_inject_stall.load();
+    prm.item_order = g_item_order.load();
     prm.rows_per_kv = prm.group * Nq;
     prm.n_mtiles = (prm.rows_per_kv + gqa::kBM - 1) / gqa::kBM;
     prm.total_rows = static_cast<int>(BHq * Nq);
@@ -798,5 +842,7 @@ void attn_test_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); 
 void attn_test_select_kernel(int which) { g_kernel_choice.store(which == 1 ? 1 : 0); }
 
 void attn_test_force_splits(int n_splits) { g_force_splits.store(n_splits > 0 ? n_splits : 0); }
+
+void attn_test_set_item_order(int order) { g_item_order.store(order == 1 ? 1 : 0); }
 
 }  // extern "C"

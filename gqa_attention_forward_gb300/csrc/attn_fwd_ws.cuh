@@ -6,10 +6,10 @@
 // (deepseek.csdn.net/6a3201f8..., sections "在线softmax" and "FlashAttention").
 //
 // Roles (384 threads):
-//   warps 2-3     loaders: K_0, (Q0, Q1), V_0, K_1, V_1, ... with 16-byte cp.async
-//                 into a ring of kStagesWs 128-byte-swizzled tiles (full / empty
-//                 mbarriers); each thread's copies arrive on the full barrier
-//                 when they land (cp.async.mbarrier.arrive).
+//   warp 2        TMA producer (one lane): K_0, (Q0, Q1), V_0, K_1, V_1, ... as
+//                 128-row boxes of 64 columns with the 128-byte swizzle, into a
+//                 ring of kStagesWs tiles (full / empty mbarriers; each full
+//                 barrier expects the tile's bytes as a transaction count).
 //   warp 1        allocates and frees the 512 TMEM columns.
 //   warp 0        MMA issuer (one lane):  S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per
 //                 key tile j:  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,
@@ -23,15 +23,22 @@
 // so P never goes through shared memory.  The commit that signals S_i(j+1)
 // also covers P_i V_j (tcgen05.commit tracks every earlier MMA), so when a
 // softmax thread sees S_i(j+1) its O_i row is stable and can be rescaled.
+// The epilogue stages each warp's rows through shared memory so that every
+// global store instruction writes whole 64-byte row segments.
 //
 // Work items are ordered longest causal row block first and dealt to the
 // persistent CTAs in a snake order (CTA c takes item r*G + c on even rounds and
 // r*G + G-1-c on odd rounds), which evens out the linearly shrinking causal
 // work; the heads of one GQA group are adjacent so their K/V reads share L2
 // (page "从零开始写Qwen3", deepseek.csdn.net/6a31faef..., "改进1-使用正确的grid").
+// A second order (kv-group major: every block of one (batch, kv head) group
+// before the next group) keeps one group's K/V in L2 at a time; measured, it
+// is slower on causal problems, so it is not the default.
 // Causal tiles above the diagonal are never loaded and only diagonal tiles are
 // masked (same page, "改进2-KV只读取下三角", "改进3-两阶段计算").
 #pragma once
+#include <cuda.h>  // CUtensorMap
+
 #include "kernel_common.cuh"
 
 namespace gqa {
@@ -55,7 +62,10 @@ struct WsLayout {
     static constexpr int kTileBytes = kAtoms * kAtomBytes;
     static constexpr int kQ = 0;  // Q0, Q1
     static constexpr int kKV = kQ + 2 * kTileBytes;
-    static constexpr int kBar = kKV + kStagesWs * kTileBytes;
+    // epilogue staging: 32 rows x 64 bytes for each of the 8 softmax warps
+    static constexpr int kStageBytes = 32 * 64;
+    static constexpr int kStage = kKV + kStagesWs * kTileBytes;
+    static constexpr int kBar = kStage + 8 * kStageBytes;
     // q_full[2], q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], mma_done
     static constexpr int kNumBars = 2 + 1 + 2 * kStagesWs + 2 + 2 + 2 + 1;
     static constexpr int kFlags = kBar + kNumBars * 8;  // split flags [2 tiles][4 warps]
@@ -80,13 +90,29 @@ struct Ring {
 };
 
 // Work item of round r for this CTA (snake order), or false past the end.
+//   item_order 0: longest row block first over all heads, the heads of a block
+//                 level adjacent (t -> qb = last - t / BHq, bh = t % BHq);
+//   item_order 1: kv-group major: all blocks of one (batch, kv head) group
+//                 before the next, longest first within the group, the group's
+//                 query heads adjacent.
 __device__ __forceinline__ bool ws_item(const Params &p, int r, int &bh, int &qb) {
-    const int G = static_cast<int>(gridDim.x);
-    const int c = (r & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-    const long long t = static_cast<long long>(r) * G + c;
-    if (t >= p.n_items) return false;
-    qb = p.n_qblocks - 1 - static_cast<int>(t / p.BHq);
-    bh = static_cast<int>(t % p.BHq);
+    // 32-bit arithmetic throughout: the host guarantees n_items <= INT_MAX, and
+    // 64-bit divisions here cost the softmax loop around them measurably.
+    const unsigned G = gridDim.x;
+    const unsigned c = (r & 1) ? (G - 1u - blockIdx.x) : blockIdx.x;
+    const unsigned t = static_cast<unsigned>(r) * G + c;
+    if (t >= static_cast<unsigned>(p.n_items)) return false;
+    const unsigned nqb = static_cast<unsigned>(p.n_qblocks);
+    if (p.item_order == 0) {
+        const unsigned bhq = static_cast<unsigned>(p.BHq);
+        qb = static_cast<int>(nqb - 1u - t / bhq);
+        bh = static_cast<int>(t % bhq);
+    } else {
+        const unsigned grp = static_cast<unsigned>(p.group), per_group = grp * nqb;
+        const unsigned g = t / per_group, rr = t - g * per_group;
+        qb = static_cast<int>(nqb - 1u - rr / grp);
+        bh = static_cast<int>(g * grp + rr % grp);
+    }
     return true;
 }
 
@@ -97,9 +123,13 @@ __device__ __forceinline__ int ws_tiles(const Params &p, int qb, int i) {
     return causal_kv_tiles(qb * 256 + 128 * i, p.Nq, p.causal_off, p.n_kv_tiles);
 }
 
+// tmQ, tmK, tmV: 3-D tensor maps (D, rows, heads) of Q [B*Hq, Nq, D] and
+// K, V [B*Hkv, Nk, D], box 64 x 128 x 1 with the 128-byte swizzle; rows past
+// the end of a head read as zeros.
 template <int D, bool kBF16, bool kCausal>
 __global__ void __launch_bounds__(kWsThreads, 1)
-    attn_fwd_ws_kernel(const Params p) {
+    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const Params p) {
     using L = WsLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -123,11 +153,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
-        mbar_init(q_full(0), kLoaderThreads);
-        mbar_init(q_full(1), kLoaderThreads);
+        mbar_init(q_full(0), 1);
+        mbar_init(q_full(1), 1);
         mbar_init(q_empty, 1);
         for (int s = 0; s < kStagesWs; ++s) {
-            mbar_init(kv_full(s), kLoaderThreads);
+            mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -151,49 +181,61 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     if (warp < 4) {
         regs_dec<kRegsLow>();
-        if (warp >= 2) {
-            // ---------------------------------------------------- loaders (warps 2, 3)
-            const int ltid = threadIdx.x - 64;
+        if (warp == 2 && lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            tma_prefetch_map(&tmQ);
+            tma_prefetch_map(&tmK);
+            tma_prefetch_map(&tmV);
             Ring ring;
             int items = 0;
             bool ok = true;
-            // Each loader thread's copies of a tile arrive on the tile's barrier as
-            // soon as they land (64 arrivals complete it).
-            auto load_kv = [&](const uint8_t *head, int row0) -> bool {
+            int kv_loads = 0;  // K/V tiles issued so far (ring position = kv_loads mod stages)
+            // One tile = D/64 boxes of 128 rows x 64 columns (128 bytes, x = 64a:
+            // a multiple of 16 bytes); the full barrier expects all of its bytes.
+            auto load_tile_tma = [&](uint32_t dst, const CUtensorMap *tm, int row, int head, uint32_t bar) {
+                mbar_arrive_expect_tx(bar, L::kTileBytes);
+#pragma unroll
+                for (int a = 0; a < L::kAtoms; ++a) tma_load_3d(dst + a * kAtomBytes, tm, 64 * a, row, head, bar);
+            };
+            auto load_kv = [&](const CUtensorMap *tm, int row, int head) -> bool {
                 if (!wait_bar(kv_empty(ring.s), ring.ph ^ 1u, p, abort_flag)) return false;
-                load_tile<D>(sKV + ring.s * L::kTileBytes, head, row0, p.Nk, ltid);
-                cp_async_arrive(kv_full(ring.s));
+                load_tile_tma(sKV + ring.s * L::kTileBytes, tm, row, head, kv_full(ring.s));
+                ++kv_loads;
                 ring.next();
                 return true;
             };
+            int q_loads = 0;
             for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
                 int bh, qb;
                 if (!ws_item(p, r, bh, qb)) continue;
-                const size_t kv_head_bytes = static_cast<size_t>(p.Nk) * D * 2;
-                const uint8_t *qh = p.q + static_cast<size_t>(bh) * p.Nq * D * 2;
-                const uint8_t *kh = p.k + static_cast<size_t>(bh / p.group) * kv_head_bytes;
-                const uint8_t *vh = p.v + static_cast<size_t>(bh / p.group) * kv_head_bytes;
+                const int kvh = bh / p.group;
                 const int q0 = qb * 256;
                 const int n1 = ws_tiles<kCausal>(p, qb, 1);
                 // K_0 may land while the previous item still runs; the Q buffers
                 // are free once every S MMA of the previous item is done.
-                if (!(ok = load_kv(kh, 0))) break;
+                if (!(ok = load_kv(&tmK, 0, kvh))) break;
                 if (!(ok = wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag))) break;
                 if (!p.inject_stall) {
-                    load_tile<D>(sQ, qh, q0, p.Nq, ltid);
-                    cp_async_arrive(q_full(0));
-                    load_tile<D>(sQ + L::kTileBytes, qh, q0 + 128, p.Nq, ltid);
-                    cp_async_arrive(q_full(1));
+                    load_tile_tma(sQ, &tmQ, q0, bh, q_full(0));
+                    load_tile_tma(sQ + L::kTileBytes, &tmQ, q0 + 128, bh, q_full(1));
+                    ++q_loads;
                 }
                 ++items;
                 for (int j = 0; j < n1 && ok; ++j) {
-                    ok = load_kv(vh, j * kBN);
-                    if (ok && j + 1 < n1) ok = load_kv(kh, (j + 1) * kBN);
+                    ok = load_kv(&tmV, j * kBN, kvh);
+                    if (ok && j + 1 < n1) ok = load_kv(&tmK, (j + 1) * kBN, kvh);
                 }
             }
-            // Every copy has landed before the CTA exits.
-            cp_async_commit();
-            cp_async_wait<0>();
+            // Every copy has landed before the CTA exits (also after a timeout).  The
+            // ring is filled in order, so stage st last received a copy in the current
+            // lap (phase ring.ph) if st < ring.s, else in the lap before.
+#pragma unroll
+            for (int st = 0; st < kStagesWs; ++st)
+                if (kv_loads > st) drain_bar(kv_full(st), st < ring.s ? ring.ph : ring.ph ^ 1u, p);
+            if (q_loads > 0) {
+                drain_bar(q_full(0), (q_loads - 1) & 1, p);
+                drain_bar(q_full(1), (q_loads - 1) & 1, p);
+            }
         } else if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, 128, kBN, false);
@@ -218,18 +260,31 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
             };
             // O_i (+)= P_i V: P_hi from the first 64 columns of S_i, and, when a
-            // softmax warp split this tile, P_lo from the next 64.
+            // softmax warp split this tile, P_lo from the next 64.  The P_lo pass
+            // writes only the lanes of the warps that split: the other warps'
+            // columns 64..127 still hold scores, which must not reach O.
             auto pv = [&](int i, int vstage, bool acc) {
                 const uint64_t b0 = dv0 + static_cast<uint64_t>(vstage * (L::kTileBytes >> 4));
                 const uint32_t ta = tmem + 128u * i, td = tmem + 256u + 128u * i;
-                const bool split = (split_flag(i, 0) | split_flag(i, 1) | split_flag(i, 2) | split_flag(i, 3)) != 0;
+                // lanes 32w..32w+31 belong to softmax warp w of the tile
+                uint32_t lo_off[4];
+                bool split = false;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const bool sw = split_flag(i, w) != 0;
+                    lo_off[w] = sw ? 0u : ~0u;
+                    split |= sw;
+                }
                 const int passes = split ? 2 : 1;
 #pragma unroll 1
-                for (int h = 0; h < passes; ++h)
+                for (int h = 0; h < passes; ++h) {
+                    const uint32_t off[4] = {h ? lo_off[0] : 0u, h ? lo_off[1] : 0u, h ? lo_off[2] : 0u,
+                                             h ? lo_off[3] : 0u};
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_f16_ts(td, ta + 64u * h + 8u * kk, b0 + kk * (2048 >> 4), idesc_pv,
-                                   (acc || kk > 0 || h > 0) ? 1u : 0u);
+                        mma_f16_ts_lanes(td, ta + 64u * h + 8u * kk, b0 + kk * (2048 >> 4), idesc_pv, off,
+                                         (acc || kk > 0 || h > 0) ? 1u : 0u);
+                }
             };
             for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
                 int bh, qb;
@@ -238,12 +293,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const uint32_t ip = items & 1;
                 if (!(ok = wait_bar(q_full(0), ip, p, abort_flag))) break;
                 if (!(ok = wait_bar(kv_full(ring.s), ring.ph, p, abort_flag))) break;
-                fence_proxy_async_smem();  // cp.async data -> tensor core reads
                 tc_fence_after();
                 qk(0, ring.s);
                 mma_commit(s_full(0));
                 if (!(ok = wait_bar(q_full(1), ip, p, abort_flag))) break;
-                fence_proxy_async_smem();
                 tc_fence_after();
                 qk(1, ring.s);
                 mma_commit(s_full(1));
@@ -252,7 +305,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 for (int j = 0; j < n1; ++j) {
                     const int vs = ring.s;
                     if (!(ok = wait_bar(kv_full(vs), ring.ph, p, abort_flag))) break;
-                    fence_proxy_async_smem();
                     ring.next();
                     if (j < n0) {
                         if (!(ok = wait_bar(p_full(0), pcount[0] & 1u, p, abort_flag))) break;
@@ -265,7 +317,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const int ks = ring.s;
                     if (more) {
                         if (!(ok = wait_bar(kv_full(ks), ring.ph, p, abort_flag))) break;
-                        fence_proxy_async_smem();
                         tc_fence_after();
                         if (j + 1 < n0) {
                             qk(0, ks);
@@ -392,18 +443,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 // weight on few keys: its running sum relative to its largest weight
                 // 2^((m_top - m_ref) c) is below kSplitL.
                 const bool need = l * ex2_approx((m_ref - m_top) * c) < kSplitL;
-                // No warpgroup-wide agreement: a warp that does not split zeroes its
-                // P_lo columns, so the P_lo V pass, which the MMA warp issues when any
-                // of the four flags is set, adds nothing to its rows.
+                // No warpgroup-wide agreement: each warp decides for its 32 rows, and
+                // the MMA warp's P_lo pass writes only the lanes of warps that split.
                 const bool split = __any_sync(0xffffffffu, need);
                 if (lane == 0) split_flag(i, wq) = split ? 1u : 0u;
-                if (!split) {
-                    uint32_t z[32];
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) z[t] = 0u;
-                    tmem_st32(tS + 64, z);
-                    tmem_st32(tS + 96, z);
-                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t pk[16];
@@ -447,22 +490,37 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             __syncwarp();
             const int row = row0 + r;
             const float inv_l = 1.f / l;  // l is in units of 2^(m_ref * c)
-            uint8_t *orow = static_cast<uint8_t *>(p.o) + (static_cast<size_t>(bh) * p.Nq + row) * (D * 2);
+            // 32 columns at a time: each thread puts its row's 64 bytes into the
+            // warp's staging rows (16-byte chunk c of row t at chunk c ^ ((t >> 1) & 3),
+            // so neither the writes nor the reads conflict on banks), then lanes
+            // 4k..4k+3 write the 64 bytes of one row: 8 whole row segments per store.
+            const uint32_t stage = base + L::kStage + static_cast<uint32_t>(warp - 4) * L::kStageBytes;
+            const int rd_row = lane >> 2, rd_c = lane & 3;  // + 8 s for s = 0..3
+            uint8_t *ohead = static_cast<uint8_t *>(p.o) + static_cast<size_t>(bh) * p.Nq * (D * 2);
+            const int wrow0 = row0 + wq * 32;  // first row of this warp
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * q, o);
                 tmem_ld_wait(o);
-                if (row < p.Nq) {
-                    uint32_t w[16];
+                uint32_t w[16];
 #pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        w[t] = pack2<kBF16>(u2f(o[2 * t]) * inv_l, u2f(o[2 * t + 1]) * inv_l);
+                for (int t = 0; t < 16; ++t)
+                    w[t] = pack2<kBF16>(u2f(o[2 * t]) * inv_l, u2f(o[2 * t + 1]) * inv_l);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        st_global_v4(orow + q * 64 + v * 16, w[4 * v], w[4 * v + 1], w[4 * v + 2],
-                                     w[4 * v + 3]);
+                for (int v = 0; v < 4; ++v)
+                    st_shared_v4(stage + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4), w[4 * v], w[4 * v + 1],
+                                 w[4 * v + 2], w[4 * v + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const int t = 8 * s4 + rd_row;  // row within the warp
+                    const uint4 x = ld_shared_v4(stage + t * 64 + ((rd_c ^ ((t >> 1) & 3)) << 4));
+                    if (wrow0 + t < p.Nq)
+                        st_global_v4(ohead + static_cast<size_t>(wrow0 + t) * (D * 2) + q * 64 + rd_c * 16, x.x, x.y,
+                                     x.z, x.w);
                 }
+                __syncwarp();
             }
             if (p.lse != nullptr && row < p.Nq)
                 p.lse[static_cast<size_t>(bh) * p.Nq + row] = (m_ref * c + log2f(l)) * 0.6931471805599453f;

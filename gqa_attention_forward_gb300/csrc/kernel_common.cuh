@@ -47,6 +47,7 @@ struct Params {
     unsigned int seq;
     unsigned long long timeout_ns;
     int inject_stall;  // test hook: the producer never loads Q
+    int item_order;    // persistent kernel: 0 head-fastest, 1 kv-group major
     // packed short-query path (attn_fwd_decode)
     int rows_per_kv;   // Hq / Hkv * Nq query rows share one kv head (contiguous in Q)
     int n_mtiles;      // ceil(rows_per_kv / kBM)

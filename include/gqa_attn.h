@@ -260,6 +260,16 @@ void attn_test_select_kernel(int which);
  * their own choice. */
 void attn_test_force_splits(int n_splits);
 
+/* attn_test_set_item_order: work-item order of the persistent kernel (the
+ * default one of attn_fwd / attn_fwd_kv).  0 (default) = the longest causal
+ * row blocks first across all heads, the query heads of a GQA group adjacent;
+ * 1 = kv-group major: every row block of one (batch, kv head) group, longest
+ * first, before the next group, so that one group's K/V is live in L2 at a
+ * time (the grid order of page "从零开始写Qwen3", deepseek.csdn.net/6a31faef...,
+ * section "改进1-使用正确的grid").  Both orders compute every item once and give
+ * the same bits; the hook exists to measure one against the other. */
+void attn_test_set_item_order(int order);
+
 #ifdef __cplusplus
 }
 #endif

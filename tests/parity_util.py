@@ -70,11 +70,15 @@ def ulp_of(x: np.ndarray, dtype: str) -> np.ndarray:
     return np.exp2(e - _FRAC_BITS[dtype])
 
 
-def ulp_error(o_gpu: np.ndarray, o_ref: np.ndarray, dtype: str) -> float:
-    """max over elements of |O_gpu - O_ref| in units of the storage type's ulp at |O_ref|."""
+def ulp_error(o_gpu: np.ndarray, o_ref: np.ndarray, dtype: str, floor: float = 1.0) -> float:
+    """max over elements of |O_gpu - O_ref| in units of the storage type's ulp at
+    max(|O_ref|, floor).  The floor (1 by default, the same floor as the LSE
+    tolerance) keeps outputs near zero, whose own ulp is tiny while their error is
+    set by the scale of V, from dominating the figure."""
     if o_ref.size == 0:
         return 0.0
-    return float(np.max(np.abs(o_gpu - o_ref) / ulp_of(o_ref, dtype)))
+    scale = np.maximum(np.abs(o_ref), floor)
+    return float(np.max(np.abs(o_gpu - o_ref) / ulp_of(scale, dtype)))
 
 
 def record(entry: dict) -> None:

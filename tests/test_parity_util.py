@@ -31,3 +31,10 @@ def test_ulp_error_is_in_units_of_the_reference():
     ref = np.array([4.0, 1.0, -0.25])
     got = ref + np.array([2.0 ** -5, 0.0, 0.0])  # one bf16 ulp at 4
     assert ulp_error(got, ref, "bf16") == 1.0
+
+
+def test_ulp_error_floors_small_outputs_at_one():
+    ref = np.array([1e-3, 2.0])
+    got = ref + np.array([2.0 ** -7, 0.0])  # one bf16 ulp of 1 on a tiny output
+    assert ulp_error(got, ref, "bf16") == 1.0
+    assert ulp_error(got, ref, "bf16", floor=0.0) > 100
