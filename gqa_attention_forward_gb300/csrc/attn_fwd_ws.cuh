@@ -221,6 +221,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     ++q_loads;
                 }
                 ++items;
+                // The next item's query rows are read from DRAM once; start bringing
+                // them into L2 now, so that their load after this item hits L2.
+                int nbh, nqb;
+                if (ws_item(p, r + 1, nbh, nqb)) {
+#pragma unroll
+                    for (int a = 0; a < L::kAtoms; ++a) {
+                        tma_prefetch_l2_3d(&tmQ, 64 * a, nqb * 256, nbh);
+                        tma_prefetch_l2_3d(&tmQ, 64 * a, nqb * 256 + 128, nbh);
+                    }
+                }
                 for (int j = 0; j < n1 && ok; ++j) {
                     ok = load_kv(&tmV, j * kBN, kvh);
                     if (ok && j + 1 < n1) ok = load_kv(&tmK, (j + 1) * kBN, kvh);
