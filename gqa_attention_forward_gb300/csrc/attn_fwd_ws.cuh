@@ -66,9 +66,8 @@ struct WsLayout {
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kStage = kKV + kStagesWs * kTileBytes;
     static constexpr int kBar = kStage + 8 * kStageBytes;
-    // q_full[2], q_empty[0], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], mma_done,
-    // q_empty[1]
-    static constexpr int kNumBars = 2 + 1 + 2 * kStagesWs + 2 + 2 + 2 + 1 + 1;
+    // q_full[2], q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], mma_done
+    static constexpr int kNumBars = 2 + 1 + 2 * kStagesWs + 2 + 2 + 2 + 1;
     static constexpr int kFlags = kBar + kNumBars * 8;  // split flags [2 tiles][4 warps]
     static constexpr int kTmemSlot = kFlags + 32;
     static constexpr int kAbort = kTmemSlot + 4;
@@ -139,8 +138,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t sQ = base + L::kQ, sKV = base + L::kKV;
     const uint32_t bar0 = base + L::kBar;
     auto q_full = [&](int i) { return bar0 + 8u * i; };
-    // Q_i's buffer is free once the item's last S_i MMA has completed
-    auto q_empty = [&](int i) { return i ? bar0 + 8u * (10 + 2 * kStagesWs) : bar0 + 8u * 2; };
+    const uint32_t q_empty = bar0 + 8u * 2;
     auto kv_full = [&](int s) { return bar0 + 8u * (3 + s); };
     auto kv_empty = [&](int s) { return bar0 + 8u * (3 + kStagesWs + s); };
     auto s_full = [&](int i) { return bar0 + 8u * (3 + 2 * kStagesWs + i); };
@@ -157,8 +155,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
         mbar_init(q_full(0), 1);
         mbar_init(q_full(1), 1);
-        mbar_init(q_empty(0), 1);
-        mbar_init(q_empty(1), 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < kStagesWs; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
@@ -207,7 +204,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 ring.next();
                 return true;
             };
-            int q0_loads = 0, q1_loads = 0;  // query tiles issued into each Q buffer
+            int q_loads = 0;
             for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
                 int bh, qb;
                 if (!ws_item(p, r, bh, qb)) continue;
@@ -217,15 +214,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 // K_0 may land while the previous item still runs; the Q buffers
                 // are free once every S MMA of the previous item is done.
                 if (!(ok = load_kv(&tmK, 0, kvh))) break;
-                if (!(ok = wait_bar(q_empty(0), (items & 1) ^ 1u, p, abort_flag))) break;
+                if (!(ok = wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag))) break;
                 if (!p.inject_stall) {
                     load_tile_tma(sQ, &tmQ, q0, bh, q_full(0));
-                    ++q0_loads;
-                }
-                if (!(ok = wait_bar(q_empty(1), (items & 1) ^ 1u, p, abort_flag))) break;
-                if (!p.inject_stall) {
                     load_tile_tma(sQ + L::kTileBytes, &tmQ, q0 + 128, bh, q_full(1));
-                    ++q1_loads;
+                    ++q_loads;
                 }
                 ++items;
                 // The next item's query rows are read from DRAM once; start bringing
@@ -249,8 +242,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
             for (int st = 0; st < kStagesWs; ++st)
                 if (kv_loads > st) drain_bar(kv_full(st), st < ring.s ? ring.ph : ring.ph ^ 1u, p);
-            if (q0_loads > 0) drain_bar(q_full(0), (q0_loads - 1) & 1, p);
-            if (q1_loads > 0) drain_bar(q_full(1), (q1_loads - 1) & 1, p);
+            if (q_loads > 0) {
+                drain_bar(q_full(0), (q_loads - 1) & 1, p);
+                drain_bar(q_full(1), (q_loads - 1) & 1, p);
+            }
         } else if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, 128, kBN, false);
@@ -311,12 +306,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after();
                 qk(0, ring.s);
                 mma_commit(s_full(0));
-                if (n0 == 1) mma_commit(q_empty(0));  // the item's only S0 MMA
                 if (!(ok = wait_bar(q_full(1), ip, p, abort_flag))) break;
                 tc_fence_after();
                 qk(1, ring.s);
                 mma_commit(s_full(1));
-                if (n1 == 1) mma_commit(q_empty(1));
                 mma_commit(kv_empty(ring.s));
                 ring.next();
                 for (int j = 0; j < n1; ++j) {
@@ -338,9 +331,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         if (j + 1 < n0) {
                             qk(0, ks);
                             mma_commit(s_full(0));
-                            // the last S0 MMA: the next item's Q0 may load while this
-                            // item finishes
-                            if (j + 2 == n0) mma_commit(q_empty(0));
                         }
                     }
                     if (!(ok = wait_bar(p_full(1), pcount[1] & 1u, p, abort_flag))) break;
@@ -352,12 +342,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     if (more) {
                         qk(1, ks);
                         mma_commit(s_full(1));
-                        if (j + 2 == n1) mma_commit(q_empty(1));
                         mma_commit(kv_empty(ks));
                         ring.next();
                     }
                 }
                 if (!ok) break;
+                mma_commit(q_empty);  // this item's S MMAs no longer read Q0, Q1
                 ++items;
             }
             // TMEM and shared memory stay alive until every issued MMA is done.
