@@ -151,8 +151,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     auto split_flag = [&](int i, int w) -> volatile uint32_t & { return flags[4 * i + w]; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    if (threadIdx.x == 64) {
+        // the producer's tensor maps: fetch the descriptors while the CTA sets up
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+    }
     if (threadIdx.x == 0) {
-        *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
+        // No global read on the way to the first copy: a CTA that starts after
+        // another one of this launch gave up learns of it in its first bounded
+        // wait (after a millisecond), like every other CTA.
+        *abort_flag = 0;
         mbar_init(q_full(0), 1);
         mbar_init(q_full(1), 1);
         mbar_init(q_empty, 1);
@@ -169,7 +178,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
-    if (*abort_flag) return;  // another CTA of this launch already gave up
     if (warp == 1) {
         tmem_alloc(base + L::kTmemSlot, kWsTmemCols);
         tmem_relinquish();
@@ -183,9 +191,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         regs_dec<kRegsLow>();
         if (warp == 2 && lane == 0) {
             // ---------------------------------------------------- TMA producer
-            tma_prefetch_map(&tmQ);
-            tma_prefetch_map(&tmK);
-            tma_prefetch_map(&tmV);
             Ring ring;
             int items = 0;
             bool ok = true;

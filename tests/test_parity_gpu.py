@@ -180,6 +180,24 @@ def test_scale_is_honoured():
     assert_parity(w, _np(o), _np(lse), ro, rl, "scale 0.05")
 
 
+@pytest.mark.parametrize("name", ["pages_shape_causal_gqa_f16", "noncausal_gqa_bf16_n4096"])
+def test_item_orders_give_the_same_bits(name):
+    """The kv-group-major work order (a measurement hook) visits the same items with the
+    same per-item arithmetic as the default order: identical O and LSE."""
+    import torch
+
+    lib = binding.load()
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    o0, l0 = run_gpu(w, x)
+    try:
+        lib.attn_test_set_item_order(1)
+        o1, l1 = run_gpu(w, x)
+    finally:
+        lib.attn_test_set_item_order(0)
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
 @pytest.fixture
 def tile_kernel():
     """Selects the one-CTA-per-query-tile kernel for the test, then restores the default."""
