@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full(i), 1);
-            mbar_init(p_full(i), 128);
+            mbar_init(p_full(i), 4);  // one arrival per softmax warp
             mbar_init(o_full(i), 1);
         }
         mbar_init(mma_done, 1);
@@ -492,7 +492,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(p_full(i));
+                // one arrival per warp once every lane's TMEM stores are done: 4 instead
+                // of 128 atomics on the barrier the MMA warp is waiting for
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(i));
             }
             if (!ok) break;
             // ---------------------------------------------------- epilogue
