@@ -71,7 +71,8 @@ def parse_args():
 ALL_WORKLOADS = [DEFAULT_WORKLOAD, "tiny_causal_gqa_f16", "pages_shape_causal_gqa_f16",
                  "noncausal_gqa_bf16_n4096", "tail_stress_causal_gqa_bf16_n2000",
                  "chunked_prefill_causal_gqa_bf16_q4096_k32768", "decode_gqa_bf16_b1_q1_k32768",
-                 "decode_gqa_bf16_b16_q1_k8192", "short_chunk_gqa_bf16_q16_k32768"]
+                 "decode_gqa_bf16_b16_q1_k8192", "short_chunk_gqa_bf16_q16_k32768",
+                 "noncausal_gqa_bf16_n4096_split", "chunked_prefill_causal_gqa_bf16_q4096_k32768_split"]
 L2_BYTES = 126 * 2 ** 20  # GB300 L2 (129 MB as the device reports it)
 FLUSH_BYTES = 256 * 2 ** 20
 
@@ -320,12 +321,19 @@ def measure(w_full, args, rank, world, device):
     dcode = binding.ATTN_BF16 if w.dtype == "bf16" else binding.ATTN_F16
     square = w.n_keys == w.N
     decode = w.entry == "attn_fwd_decode"
+    split = w.entry == "attn_fwd_kv_split"
     workspace, ws_bytes = None, 0
     if decode and has_work:
         st, ws_bytes = binding.attn_fwd_decode_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D)
         if st != binding.ATTN_OK:
             raise binding.AttnError(st, "attn_fwd_decode_workspace")
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    if split and has_work:
+        st, ws_bytes = binding.attn_fwd_kv_split_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
+                                                           w.causal)
+        if st != binding.ATTN_OK:
+            raise binding.AttnError(st, "attn_fwd_kv_split_workspace")
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
 
     def launch():
         if not has_work:
@@ -334,6 +342,9 @@ def measure(w_full, args, rank, world, device):
         if decode:
             st = binding.attn_fwd_decode(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
                                          w.scale, w.causal, dcode, workspace, ws_bytes, s_now)
+        elif split:
+            st = binding.attn_fwd_kv_split(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
+                                           w.scale, w.causal, dcode, workspace, ws_bytes, s_now)
         elif square:
             st = binding.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.D, w.scale, w.causal,
                                   dcode, s_now)
@@ -341,7 +352,8 @@ def measure(w_full, args, rank, world, device):
             st = binding.attn_fwd_kv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
                                      w.scale, w.causal, dcode, s_now)
         if st != binding.ATTN_OK:
-            raise binding.AttnError(st, w.entry if decode else ("attn_fwd" if square else "attn_fwd_kv"))
+            raise binding.AttnError(st, w.entry if (decode or split) else
+                                    ("attn_fwd" if square else "attn_fwd_kv"))
 
     step = launch
     host_us = None
@@ -430,7 +442,7 @@ def measure(w_full, args, rank, world, device):
     def e2e_step():
         if not has_work:
             return
-        if decode:
+        if decode or split:
             dq.copy_(hq.view(-1), non_blocking=True)
             dk.copy_(hk.view(-1), non_blocking=True)
             dv.copy_(hv.view(-1), non_blocking=True)
@@ -507,9 +519,9 @@ def measure(w_full, args, rank, world, device):
         "e2e": {"value": round(job_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
-                "path": ("torch copies around attn_fwd_decode" if decode else
+                "path": (f"torch copies around {w.entry}" if (decode or split) else
                          "attn_fwd_host: pinned host buffers, chunked copies overlapping compute")},
-        "gpu_launches": K * (2 if ws_bytes else 1) * (1 if has_work else 0),
+        "gpu_launches": K * (2 if (decode and ws_bytes) else 1) * (1 if has_work else 0),
         "launch": {"mode": "cuda_graph_replay" if args.graph else "direct",
                    "host_us_per_call": None if host_us is None else round(host_us, 2)},
         "clocks": clock_info,

@@ -56,6 +56,11 @@ def load(path: str | None = None):
         lib.attn_fwd_host.restype = i
         lib.attn_fwd_decode_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_fwd_decode_workspace.restype = i
+        lib.attn_fwd_kv_split.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, i,
+                                          vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_kv_split.restype = i
+        lib.attn_fwd_kv_split_workspace.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_fwd_kv_split_workspace.restype = i
         lib.attn_test_force_splits.argtypes = [i]
         lib.attn_test_force_splits.restype = None
         lib.attn_status_str.argtypes = [i]
@@ -132,6 +137,24 @@ def attn_fwd_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype
                                _stream_handle(stream))
 
 
+def attn_fwd_kv_split(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, workspace,
+                      workspace_bytes, stream=None) -> int:
+    """The C entry point with the same name; returns its status code."""
+    lib = load()
+    return lib.attn_fwd_kv_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                                 int(Hkv), int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
+                                 _dtype_code(dtype), _ptr(workspace), int(workspace_bytes),
+                                 _stream_handle(stream))
+
+
+def attn_fwd_kv_split_workspace(B, Hq, Hkv, Nq, Nk, D, causal):
+    """(status, bytes) of the C entry point with the same name."""
+    n = ctypes.c_size_t(0)
+    st = load().attn_fwd_kv_split_workspace(int(B), int(Hq), int(Hkv), int(Nq), int(Nk), int(D),
+                                            int(bool(causal)), ctypes.byref(n))
+    return st, n.value
+
+
 def attn_fwd_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
                             stream=None) -> int:
     """The C entry point with the same name; returns its status code."""
@@ -191,6 +214,41 @@ def attention_decode(q, k, v, causal: bool = True, scale: float | None = None,
                          workspace, workspace.numel(), stream)
     if st != ATTN_OK:
         raise AttnError(st, f"attn_fwd_decode ({attn_last_cuda_error()})")
+    return o, lse
+
+
+def attention_split(q, k, v, causal: bool = True, scale: float | None = None, with_lse: bool = True,
+                    workspace=None, out=None, lse_out=None, stream=None):
+    """attn_fwd_kv_split for torch CUDA tensors q [B,Hq,Nq,D], k/v [B,Hkv,Nk,D].
+
+    ``workspace``: a uint8 CUDA tensor (256-byte aligned, as torch allocates), or
+    None to let torch allocate the size attn_fwd_kv_split_workspace asks for.
+    Returns (o, lse) without waiting."""
+    import torch
+
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous [B, H, N, D]")
+    o = out if out is not None else torch.empty_like(q)
+    lse = None
+    if with_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, Hq, Nq), dtype=torch.float32,
+                                                              device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if workspace is None:
+        st, nbytes = attn_fwd_kv_split_workspace(B, Hq, Hkv, Nq, Nk, D, causal)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_fwd_kv_split_workspace")
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_fwd_kv_split(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, q.dtype,
+                           workspace, workspace.numel(), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, f"attn_fwd_kv_split ({attn_last_cuda_error()})")
     return o, lse
 
 

@@ -453,7 +453,7 @@ attn_status_t launch(int dev, int kid, const gqa::Params &prm, cudaStream_t stre
             return ATTN_ERR_LAUNCH;
         }
         const int sms = g_dev_sms[dev];
-        const unsigned grid = static_cast<unsigned>(prm.n_items < sms ? prm.n_items : sms);
+        const unsigned grid = static_cast<unsigned>(prm.n_units < sms ? prm.n_units : sms);
         kern<<<grid, gqa::kWsThreads, smem, stream>>>(tq, tk, tv, prm);
     } else {
         auto kern = gqa::attn_fwd_kernel<D, BF16, CAUSAL>;
@@ -547,6 +547,9 @@ attn_status_t prepare(const void *q, const void *k, const void *v, void *o, floa
     prm.BHq = static_cast<int>(BHq);
     prm.n_qblocks = (Nq + 255) / 256;
     prm.n_items = static_cast<int>(BHq * prm.n_qblocks);
+    prm.n_units = prm.n_items;  // whole items only unless a split plan says otherwise
+    prm.n_whole = prm.n_items;
+    prm.n_parts = 1;
     prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     prm.seq = g_launch_seq.fetch_add(1);
     prm.timeout_ns = g_timeout_ns.load();
@@ -600,6 +603,68 @@ attn_status_t run_decode(gqa::Params &prm, int dev, int D, attn_dtype_t dtype, i
     }
 }
 
+// Key-split plan of the persistent kernel (attn_fwd_kv_split).  Items are dealt in
+// rounds of `grid` = min(items, SMs); when the last round holds at most half a round,
+// each of its R items is cut into n_parts = SMs / R key ranges (at most kMaxParts), so
+// that round runs more, shorter units.  Every range must start with a key tile that no
+// row of the item masks: n_parts is at most the number of such tiles of the item
+// (causal: tiles before the first one masked for the item's first query tile;
+// non-causal: the full tiles).  Fills n_whole / n_parts / n_units; returns the number
+// of cut items (0: no split).
+constexpr int kMaxParts = gqa::kMaxPartsWs;
+int plan_last_round(gqa::Params &prm, int sms, int causal) {
+    const long long G = prm.n_items < sms ? prm.n_items : sms;
+    const long long rounds = (prm.n_items + G - 1) / G;
+    const long long R = prm.n_items - (rounds - 1) * G;  // items of the last round
+    if (R <= 0 || 2 * R > sms) return 0;
+    int np = static_cast<int>(sms / R);
+    if (np > kMaxParts) np = kMaxParts;
+    // The cut items are the last R of the item order.  Part s of np takes the key
+    // tiles [s n0 / np, (s+1) n0 / np) of the item's first query tile (n0 of them):
+    // np is lowered until, for every cut item, each part has a tile and starts before
+    // the first tile that a row of the item masks.
+    auto fits = [&](int parts) {
+        for (long long t = prm.n_items - R; t < prm.n_items; ++t) {
+            int qb;
+            if (prm.item_order == 0) {
+                qb = prm.n_qblocks - 1 - static_cast<int>(t / prm.BHq);
+            } else {
+                const long long per_group = static_cast<long long>(prm.group) * prm.n_qblocks;
+                qb = prm.n_qblocks - 1 - static_cast<int>((t % per_group) / prm.group);
+            }
+            const int row0 = qb * 256;
+            int n0 = prm.n_kv_tiles, first_masked = prm.Nk / gqa::kBN;
+            if (causal) {
+                const int last_row = row0 + gqa::kBM - 1 < prm.Nq - 1 ? row0 + gqa::kBM - 1 : prm.Nq - 1;
+                n0 = (last_row + prm.causal_off) / gqa::kBN + 1;
+                if (n0 > prm.n_kv_tiles) n0 = prm.n_kv_tiles;
+                first_masked = (row0 + prm.causal_off + 1) / gqa::kBN;
+            }
+            if (n0 < parts || static_cast<long long>(parts - 1) * n0 / parts >= first_masked) return false;
+        }
+        return true;
+    };
+    while (np >= 2 && !fits(np)) --np;
+    if (np < 2) return 0;
+    prm.n_parts = np;
+    prm.n_whole = static_cast<int>(prm.n_items - R);
+    prm.n_units = static_cast<int>(prm.n_whole + R * np);
+    return static_cast<int>(R);
+}
+
+// Workspace layout of a split plan with `cut` items: partial outputs, then partial
+// log-sum-exps, then the arrival counters (each part 256-byte aligned).
+size_t split_ws_bytes(int cut, int parts, int D, size_t *off_lse, size_t *off_cnt) {
+    auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    const size_t rows = static_cast<size_t>(cut) * parts * 2 * gqa::kBM;
+    const size_t o = up(rows * D * sizeof(float));
+    const size_t l = up(rows * sizeof(float));
+    const size_t c = up(static_cast<size_t>(cut) * 2 * 4 * sizeof(unsigned int));
+    if (off_lse) *off_lse = o;
+    if (off_cnt) *off_cnt = o + l;
+    return o + l + c;
+}
+
 attn_status_t host_pipe(int dev, HostPipe *&pipe) {
     HostPipe &hp = g_pipe[dev];
     if (!hp.ready) {
@@ -633,6 +698,60 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
     bool empty = false;
     attn_status_t st = prepare(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm, dev, empty);
     if (st != ATTN_OK || empty) return st;
+    const bool bf16 = dtype == ATTN_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+    switch (kid) {
+        case 0: return launch<64, false, false>(dev, kid, prm, s);
+        case 1: return launch<64, false, true>(dev, kid, prm, s);
+        case 2: return launch<64, true, false>(dev, kid, prm, s);
+        case 3: return launch<64, true, true>(dev, kid, prm, s);
+        case 4: return launch<128, false, false>(dev, kid, prm, s);
+        case 5: return launch<128, false, true>(dev, kid, prm, s);
+        case 6: return launch<128, true, false>(dev, kid, prm, s);
+        default: return launch<128, true, true>(dev, kid, prm, s);
+    }
+}
+
+attn_status_t attn_fwd_kv_split_workspace(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal,
+                                          size_t *bytes) {
+    if (bytes == nullptr) return ATTN_ERR_NULL;
+    *bytes = 0;
+    static const uint8_t dummy[16] = {};
+    gqa::Params prm;
+    int dev = 0;
+    bool empty = false;
+    // validate with stand-in pointers: only the sizes matter here
+    const void *fake = reinterpret_cast<const void *>((reinterpret_cast<uintptr_t>(dummy) + 15) & ~uintptr_t(15));
+    attn_status_t st = prepare(fake, fake, fake, const_cast<void *>(fake), nullptr, B, Hq, Hkv, Nq, Nk, D, 1.f,
+                               causal, ATTN_BF16, prm, dev, empty);
+    if (st != ATTN_OK || empty) return st;
+    const int cut = plan_last_round(prm, g_dev_sms[dev], causal);
+    *bytes = cut > 0 ? split_ws_bytes(cut, prm.n_parts, D, nullptr, nullptr) : 0;
+    return ATTN_OK;
+}
+
+attn_status_t attn_fwd_kv_split(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                                int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                                attn_dtype_t dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGN;
+    gqa::Params prm;
+    int dev = 0;
+    bool empty = false;
+    attn_status_t st = prepare(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, prm, dev, empty);
+    if (st != ATTN_OK || empty) return st;
+    if (workspace != nullptr && g_kernel_choice.load() == 0) {
+        gqa::Params plan = prm;
+        const int cut = plan_last_round(plan, g_dev_sms[dev], causal);
+        size_t off_lse = 0, off_cnt = 0;
+        if (cut > 0 && split_ws_bytes(cut, plan.n_parts, D, &off_lse, &off_cnt) <= workspace_bytes) {
+            prm = plan;
+            uint8_t *w = static_cast<uint8_t *>(workspace);
+            prm.part_o = reinterpret_cast<float *>(w);
+            prm.part_lse = reinterpret_cast<float *>(w + off_lse);
+            prm.part_count = reinterpret_cast<unsigned int *>(w + off_cnt);
+        }
+    }
     const bool bf16 = dtype == ATTN_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kid = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);

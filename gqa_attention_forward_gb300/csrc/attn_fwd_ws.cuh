@@ -53,6 +53,8 @@ constexpr float kSplitL = 16.f;
 // The probabilities are referenced to a stale row max until the true max
 // exceeds it by more than this many powers of two (P <= 2^8 meanwhile).
 constexpr float kRescaleLog2 = 8.f;
+// at most this many key ranges per cut item (attn_fwd_kv_split)
+constexpr int kMaxPartsWs = 8;
 constexpr uint32_t kRegsLow = 104;   // warps 0-3 after the hand-off
 constexpr uint32_t kRegsHigh = 200;  // softmax warpgroups after the hand-off (128*104 + 256*200 <= 384*168)
 
@@ -95,13 +97,29 @@ struct Ring {
 //   item_order 1: kv-group major: all blocks of one (batch, kv head) group
 //                 before the next, longest first within the group, the group's
 //                 query heads adjacent.
-__device__ __forceinline__ bool ws_item(const Params &p, int r, int &bh, int &qb) {
-    // 32-bit arithmetic throughout: the host guarantees n_items <= INT_MAX, and
+//
+// A work unit is a whole item, or (attn_fwd_kv_split) one of n_parts key ranges of
+// an item: units [0, n_whole) are the first n_whole items, and the items after them
+// (the last round of a schedule of equal-length items) are cut into n_parts units
+// each, so that the last round has more, shorter units.  part = -1 for a whole item;
+// x numbers the cut items.
+__device__ __forceinline__ bool ws_item(const Params &p, int r, int &bh, int &qb, int &part, int &x) {
+    // 32-bit arithmetic throughout: the host guarantees n_units <= INT_MAX, and
     // 64-bit divisions here cost the softmax loop around them measurably.
     const unsigned G = gridDim.x;
     const unsigned c = (r & 1) ? (G - 1u - blockIdx.x) : blockIdx.x;
-    const unsigned t = static_cast<unsigned>(r) * G + c;
-    if (t >= static_cast<unsigned>(p.n_items)) return false;
+    const unsigned u = static_cast<unsigned>(r) * G + c;
+    if (u >= static_cast<unsigned>(p.n_units)) return false;
+    unsigned t = u;
+    part = -1;
+    x = 0;
+    if (u >= static_cast<unsigned>(p.n_whole)) {
+        const unsigned v = u - static_cast<unsigned>(p.n_whole), np = static_cast<unsigned>(p.n_parts);
+        const unsigned xx = v / np;
+        part = static_cast<int>(v - xx * np);
+        x = static_cast<int>(xx);
+        t = static_cast<unsigned>(p.n_whole) + xx;
+    }
     const unsigned nqb = static_cast<unsigned>(p.n_qblocks);
     if (p.item_order == 0) {
         const unsigned bhq = static_cast<unsigned>(p.BHq);
@@ -121,6 +139,38 @@ template <bool kCausal>
 __device__ __forceinline__ int ws_tiles(const Params &p, int qb, int i) {
     if (!kCausal) return p.n_kv_tiles;
     return causal_kv_tiles(qb * 256 + 128 * i, p.Nq, p.causal_off, p.n_kv_tiles);
+}
+
+// Key tiles of a unit: query tile 0 visits [k0, e0), query tile 1 [k0, e1).  A whole
+// item starts at 0; part s of n_parts of an item takes tiles [s n0 / np, (s+1) n0 / np)
+// of query tile 0's n0, the same range for query tile 1, and the last part also query
+// tile 1's tiles past n0.  The host keeps np small enough that every part starts with
+// a tile that no row masks.
+struct KeyRange {
+    int k0, e0, e1;
+};
+template <bool kCausal>
+__device__ __forceinline__ KeyRange ws_range(const Params &p, int qb, int part) {
+    const int n0 = ws_tiles<kCausal>(p, qb, 0), n1 = ws_tiles<kCausal>(p, qb, 1);
+    if (part < 0) return {0, n0, n1};
+    const int k0 = part * n0 / p.n_parts, e0 = (part + 1) * n0 / p.n_parts;
+    return {k0, e0, part == p.n_parts - 1 ? n1 : e0};
+}
+
+// Counts one arrival on a counter that keeps the launch's sequence number in its
+// upper 24 bits, so that a value left by another launch (or never written) counts as
+// no arrival.  Returns true for the arrival that brings the count to n, which also
+// puts the counter back at zero arrivals of this launch (ready for a graph replay).
+__device__ __forceinline__ bool arrive_last(unsigned int *ctr, unsigned int seq, int n) {
+    const unsigned int tag = (seq & 0xFFFFFFu) << 8;
+    unsigned int old = *reinterpret_cast<volatile unsigned int *>(ctr);
+    for (;;) {
+        const unsigned int cnt = ((old & ~0xFFu) == tag) ? (old & 0xFFu) : 0u;
+        const bool last = cnt + 1u == static_cast<unsigned int>(n);
+        const unsigned int prev = atomicCAS(ctr, old, last ? tag : (tag | (cnt + 1u)));
+        if (prev == old) return last;
+        old = prev;
+    }
 }
 
 // tmQ, tmK, tmV: 3-D tensor maps (D, rows, heads) of Q [B*Hq, Nq, D] and
@@ -210,15 +260,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 return true;
             };
             int q_loads = 0;
-            for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
-                int bh, qb;
-                if (!ws_item(p, r, bh, qb)) continue;
+            for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_units; ++r) {
+                int bh, qb, part, x;
+                if (!ws_item(p, r, bh, qb, part, x)) continue;
                 const int kvh = bh / p.group;
                 const int q0 = qb * 256;
-                const int n1 = ws_tiles<kCausal>(p, qb, 1);
-                // K_0 may land while the previous item still runs; the Q buffers
-                // are free once every S MMA of the previous item is done.
-                if (!(ok = load_kv(&tmK, 0, kvh))) break;
+                const KeyRange kr = ws_range<kCausal>(p, qb, part);
+                // The first K tile may land while the previous unit still runs; the Q
+                // buffers are free once every S MMA of the previous unit is done.
+                if (!(ok = load_kv(&tmK, kr.k0 * kBN, kvh))) break;
                 if (!(ok = wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag))) break;
                 if (!p.inject_stall) {
                     load_tile_tma(sQ, &tmQ, q0, bh, q_full(0));
@@ -228,17 +278,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 ++items;
                 // The next item's query rows are read from DRAM once; start bringing
                 // them into L2 now, so that their load after this item hits L2.
-                int nbh, nqb;
-                if (ws_item(p, r + 1, nbh, nqb)) {
+                int nbh, nqb, npart, nx;
+                if (ws_item(p, r + 1, nbh, nqb, npart, nx)) {
 #pragma unroll
                     for (int a = 0; a < L::kAtoms; ++a) {
                         tma_prefetch_l2_3d(&tmQ, 64 * a, nqb * 256, nbh);
                         tma_prefetch_l2_3d(&tmQ, 64 * a, nqb * 256 + 128, nbh);
                     }
                 }
-                for (int j = 0; j < n1 && ok; ++j) {
+                for (int j = kr.k0; j < kr.e1 && ok; ++j) {
                     ok = load_kv(&tmV, j * kBN, kvh);
-                    if (ok && j + 1 < n1) ok = load_kv(&tmK, (j + 1) * kBN, kvh);
+                    if (ok && j + 1 < kr.e1) ok = load_kv(&tmK, (j + 1) * kBN, kvh);
                 }
             }
             // Every copy has landed before the CTA exits (also after a timeout).  The
@@ -301,10 +351,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                          (acc || kk > 0 || h > 0) ? 1u : 0u);
                 }
             };
-            for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_items; ++r) {
-                int bh, qb;
-                if (!ws_item(p, r, bh, qb)) continue;
-                const int n0 = ws_tiles<kCausal>(p, qb, 0), n1 = ws_tiles<kCausal>(p, qb, 1);
+            for (int r = 0; ok && static_cast<long long>(r) * gridDim.x < p.n_units; ++r) {
+                int bh, qb, part, x;
+                if (!ws_item(p, r, bh, qb, part, x)) continue;
+                const KeyRange kr = ws_range<kCausal>(p, qb, part);
+                const int k0 = kr.k0, n0 = kr.e0, n1 = kr.e1;  // tiles [k0, n0) and [k0, n1)
                 const uint32_t ip = items & 1;
                 if (!(ok = wait_bar(q_full(0), ip, p, abort_flag))) break;
                 if (!(ok = wait_bar(kv_full(ring.s), ring.ph, p, abort_flag))) break;
@@ -317,7 +368,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 mma_commit(s_full(1));
                 mma_commit(kv_empty(ring.s));
                 ring.next();
-                for (int j = 0; j < n1; ++j) {
+                for (int j = k0; j < n1; ++j) {
                     const int vs = ring.s;
                     if (!(ok = wait_bar(kv_full(vs), ring.ph, p, abort_flag))) break;
                     ring.next();
@@ -325,7 +376,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         if (!(ok = wait_bar(p_full(0), pcount[0] & 1u, p, abort_flag))) break;
                         ++pcount[0];
                         tc_fence_after();
-                        pv(0, vs, j > 0);
+                        pv(0, vs, j > k0);
                         if (j == n0 - 1) mma_commit(o_full(0));
                     }
                     const bool more = j + 1 < n1;
@@ -341,7 +392,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     if (!(ok = wait_bar(p_full(1), pcount[1] & 1u, p, abort_flag))) break;
                     ++pcount[1];
                     tc_fence_after();
-                    pv(1, vs, j > 0);
+                    pv(1, vs, j > k0);
                     if (j == n1 - 1) mma_commit(o_full(1));
                     mma_commit(kv_empty(vs));
                     if (more) {
@@ -373,10 +424,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         uint32_t scount = 0;
         int items = 0;
         bool ok = true;
-        for (int rr = 0; ok && static_cast<long long>(rr) * gridDim.x < p.n_items; ++rr) {
-            int bh, qb;
-            if (!ws_item(p, rr, bh, qb)) continue;
-            const int n = ws_tiles<kCausal>(p, qb, i);
+        for (int rr = 0; ok && static_cast<long long>(rr) * gridDim.x < p.n_units; ++rr) {
+            int bh, qb, part, x;
+            if (!ws_item(p, rr, bh, qb, part, x)) continue;
+            const KeyRange kr = ws_range<kCausal>(p, qb, part);
+            const int jend = i ? kr.e1 : kr.e0;   // key tiles [kr.k0, jend) of this query tile
             const int row0 = qb * 256 + 128 * i;  // first query row of this tile
             // Causal: key tile j needs a mask unless its last key is visible to
             // row0, i.e. from tile (row0 + Nk - Nq + 1) / 128 on.
@@ -384,7 +436,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             // m_ref: the max the probabilities are taken against (updated lazily);
             // m_top: the true running row max; l: running sum in units of 2^(m_ref*c).
             float m_ref = -INFINITY, m_top = -INFINITY, l = 0.f;
-            for (int j = 0; j < n; ++j) {
+            for (int j = kr.k0; j < jend; ++j) {
                 if (!__all_sync(0xffffffffu, wait_bar(s_full(i), scount & 1u, p, abort_flag))) {
                     ok = false;
                     break;
@@ -507,7 +559,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             tc_fence_after();
             __syncwarp();
             const int row = row0 + r;
-            const float inv_l = 1.f / l;  // l is in units of 2^(m_ref * c)
             // 32 columns at a time: each thread puts its row's 64 bytes into the
             // warp's staging rows (16-byte chunk c of row t at chunk c ^ ((t >> 1) & 3),
             // so neither the writes nor the reads conflict on banks), then lanes
@@ -516,15 +567,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const int rd_row = lane >> 2, rd_c = lane & 3;  // + 8 s for s = 0..3
             uint8_t *ohead = static_cast<uint8_t *>(p.o) + static_cast<size_t>(bh) * p.Nq * (D * 2);
             const int wrow0 = row0 + wq * 32;  // first row of this warp
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t o[32];
-                tmem_ld32(tO + 32 * q, o);
-                tmem_ld_wait(o);
-                uint32_t w[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    w[t] = pack2<kBF16>(u2f(o[2 * t]) * inv_l, u2f(o[2 * t + 1]) * inv_l);
+            auto store_cols = [&](int q, const uint32_t (&w)[16]) {
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
                     st_shared_v4(stage + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4), w[4 * v], w[4 * v + 1],
@@ -533,15 +576,99 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
                 for (int s4 = 0; s4 < 4; ++s4) {
                     const int t = 8 * s4 + rd_row;  // row within the warp
-                    const uint4 x = ld_shared_v4(stage + t * 64 + ((rd_c ^ ((t >> 1) & 3)) << 4));
+                    const uint4 xv = ld_shared_v4(stage + t * 64 + ((rd_c ^ ((t >> 1) & 3)) << 4));
                     if (wrow0 + t < p.Nq)
-                        st_global_v4(ohead + static_cast<size_t>(wrow0 + t) * (D * 2) + q * 64 + rd_c * 16, x.x, x.y,
-                                     x.z, x.w);
+                        st_global_v4(ohead + static_cast<size_t>(wrow0 + t) * (D * 2) + q * 64 + rd_c * 16, xv.x,
+                                     xv.y, xv.z, xv.w);
                 }
                 __syncwarp();
+            };
+            if (part < 0) {
+                const float inv_l = 1.f / l;  // l is in units of 2^(m_ref * c)
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * q, o);
+                    tmem_ld_wait(o);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        w[t] = pack2<kBF16>(u2f(o[2 * t]) * inv_l, u2f(o[2 * t + 1]) * inv_l);
+                    store_cols(q, w);
+                }
+                if (p.lse != nullptr && row < p.Nq)
+                    p.lse[static_cast<size_t>(bh) * p.Nq + row] = (m_ref * c + log2f(l)) * 0.6931471805599453f;
+            } else {
+                // One key range of a cut item: this warp's rows of O / l (fp32) and their
+                // log-sum-exp go to the workspace; the warp that brings the last of the
+                // n_parts pieces of these rows merges them, with weights
+                // exp(lse_s - lse), lse = log sum_s exp(lse_s) (the online-softmax
+                // update of page "从零开始写Qwen3", deepseek.csdn.net/6a3201f8...,
+                // section "在线softmax", applied across CTAs).
+                // Pieces are stored column-major per (cut item, part, tile): element (d, r)
+                // at d * 128 + r, so that a warp's row-per-thread accesses are 128
+                // contiguous bytes.
+                const size_t tile_stride = static_cast<size_t>(2) * 128;  // lse entries per part
+                const size_t lse0 = (static_cast<size_t>(x) * p.n_parts * 2 + i) * 128 + r;  // part 0
+                const float *po0 = p.part_o + (static_cast<size_t>(x) * p.n_parts * 2 + i) * 128 * D + r;
+                const size_t part_stride = tile_stride * D;  // floats between parts' pieces
+                float *po = p.part_o + ((static_cast<size_t>(x) * p.n_parts + part) * 2 + i) * 128 * D + r;
+                const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * q, o);
+                    tmem_ld_wait(o);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) po[(32 * q + t) * 128] = u2f(o[t]) * inv_l;
+                }
+                p.part_lse[lse0 + part * tile_stride] = l > 0.f ? (m_ref * c + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                __threadfence();  // this warp's pieces are visible before its arrival counts
+                __syncwarp();
+                unsigned int last = 0;
+                if (lane == 0)
+                    last = arrive_last(p.part_count + (static_cast<size_t>(x) * 2 + i) * 4 + wq, p.seq, p.n_parts)
+                               ? 1u : 0u;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();  // every piece arrived before this: read them from L2
+                    // weights exp(lse_s - lse) once, in registers (kMaxParts bounds the parts)
+                    float wgt[kMaxPartsWs];
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int sp = 0; sp < kMaxPartsWs; ++sp) {
+                        wgt[sp] = sp < p.n_parts ? __ldcg(p.part_lse + lse0 + sp * tile_stride) : -INFINITY;
+                        mx = fmaxf(mx, wgt[sp]);
+                    }
+                    float sum = 0.f;
+#pragma unroll
+                    for (int sp = 0; sp < kMaxPartsWs; ++sp) {
+                        wgt[sp] = wgt[sp] == -INFINITY ? 0.f : expf(wgt[sp] - mx);
+                        sum += wgt[sp];
+                    }
+                    const float lse_all = mx + logf(sum), inv_sum = 1.f / sum;
+#pragma unroll 1
+                    for (int q = 0; q < D / 32; ++q) {
+                        float acc[32];
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) acc[t] = 0.f;
+#pragma unroll
+                        for (int sp = 0; sp < kMaxPartsWs; ++sp) {
+                            if (sp < p.n_parts) {
+                                const float *src = po0 + sp * part_stride + static_cast<size_t>(32 * q) * 128;
+                                const float ww = wgt[sp] * inv_sum;
+#pragma unroll
+                                for (int t = 0; t < 32; ++t) acc[t] += ww * __ldcg(src + t * 128);
+                            }
+                        }
+                        uint32_t w[16];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) w[t] = pack2<kBF16>(acc[2 * t], acc[2 * t + 1]);
+                        store_cols(q, w);
+                    }
+                    if (p.lse != nullptr && row < p.Nq) p.lse[static_cast<size_t>(bh) * p.Nq + row] = lse_all;
+                }
             }
-            if (p.lse != nullptr && row < p.Nq)
-                p.lse[static_cast<size_t>(bh) * p.Nq + row] = (m_ref * c + log2f(l)) * 0.6931471805599453f;
             // O_i is read; the next item's first P_i V MMA waits for this warpgroup's p_full.
             tc_fence_before();
         }

@@ -48,6 +48,14 @@ struct Params {
     unsigned long long timeout_ns;
     int inject_stall;  // test hook: the producer never loads Q
     int item_order;    // persistent kernel: 0 head-fastest, 1 kv-group major
+    // persistent kernel, key-split work units (attn_fwd_kv_split): units [0, n_whole)
+    // are whole items; every item from n_whole on is cut into n_parts key ranges
+    int n_units;       // n_whole + (n_items - n_whole) * n_parts
+    int n_whole;
+    int n_parts;
+    float *part_o;     // [split items][n_parts][2 tiles][128 rows][D] partial outputs (O / l)
+    float *part_lse;   // [split items][n_parts][2 tiles][128 rows] partial log-sum-exp
+    unsigned int *part_count;  // [split items][2 tiles][4 warps] arrivals, tagged with the launch
     // packed short-query path (attn_fwd_decode)
     int rows_per_kv;   // Hq / Hkv * Nq query rows share one kv head (contiguous in Q)
     int n_mtiles;      // ceil(rows_per_kv / kBM)

@@ -36,7 +36,7 @@ class Workload:
     v_std: float = 1.0
     seed: int = 1234
     Nk: int | None = None  # keys per head when it differs from the N query rows
-    entry: str = "attn_fwd"  # C entry point that computes it ("attn_fwd" or "attn_fwd_decode")
+    entry: str = "attn_fwd"  # C entry point: "attn_fwd", "attn_fwd_decode" or "attn_fwd_kv_split"
 
     @property
     def n_keys(self) -> int:
@@ -80,6 +80,12 @@ WORKLOADS = {
                  Nk=8192, entry="attn_fwd_decode"),
         Workload("short_chunk_gqa_bf16_q16_k32768", 1, 32, 8, 16, 128, "bf16", True, seed=1242,
                  Nk=32768, entry="attn_fwd_decode"),
+        # the equal-length workloads through attn_fwd_kv_split (last round cut along the
+        # keys); same shapes and inputs as their plain entries above
+        Workload("noncausal_gqa_bf16_n4096_split", 4, 32, 8, 4096, 128, "bf16", False, seed=1236,
+                 entry="attn_fwd_kv_split"),
+        Workload("chunked_prefill_causal_gqa_bf16_q4096_k32768_split", 1, 32, 8, 4096, 128, "bf16",
+                 True, seed=1239, Nk=32768, entry="attn_fwd_kv_split"),
     ]
 }
 ORDER = list(WORKLOADS)

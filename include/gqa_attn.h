@@ -113,6 +113,41 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
                           int causal, attn_dtype_t dtype, void *stream);
 
 /*
+ * attn_fwd_kv_split -- attn_fwd_kv with a caller workspace that lets the library
+ * balance the last round of its schedule.
+ *
+ * The persistent kernel deals 256-row items to one CTA per SM in rounds.  When
+ * every item has the same length (no mask, or a chunk of queries over a much
+ * longer key sequence) and the last round holds at most half a round of items,
+ * each of those items is cut into up to 8 key ranges; the pieces (the partial
+ * O / l in fp32 and the partial log-sum-exp of every row) go to the workspace,
+ * and the warp that computes the last piece of its rows merges them:
+ * lse = log sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s -- the online-softmax
+ * update of page "从零开始写Qwen3" (deepseek.csdn.net/6a3201f8..., section
+ * "在线softmax"), applied across CTAs.  The result equals attn_fwd_kv's up to
+ * rounding.
+ *
+ * Arguments, layout, masks and errors: as attn_fwd_kv, plus
+ * workspace        device pointer, 256-byte aligned, or NULL; workspace_bytes its
+ *                  size.  attn_fwd_kv_split_workspace gives the size the plan needs
+ *                  (0 when nothing is cut, e.g. causal problems with Nq == Nk,
+ *                  whose items already differ in length).  With a NULL or smaller
+ *                  workspace, or when nothing is cut, the call is attn_fwd_kv.
+ * Contents: the workspace needs no initial value; its counters carry the launch's
+ *   sequence number, so stale contents are recognised.  A captured call replays
+ *   correctly as long as no replay of it has timed out (ATTN_ERR_TIMEOUT); after a
+ *   timeout, capture the call again or clear the workspace.
+ * Races: calls that can run at the same time must not share a workspace.
+ * ATTN_ERR_ALIGN also when workspace is not 256-byte aligned.
+ */
+attn_status_t attn_fwd_kv_split_workspace(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal,
+                                          size_t *bytes);
+attn_status_t attn_fwd_kv_split(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+                                int causal, attn_dtype_t dtype, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
  * attn_fwd_decode -- the same function as attn_fwd_kv, computed by a kernel
  * for short query blocks over long key sequences (decode steps, small chunks).
  *

@@ -553,3 +553,138 @@ def test_random_problems_all_entry_points(prob):
     assert_parity(w, _np(o2), _np(l2), ro, rl, f"{prob} attn_fwd_decode")
     oh, lh, _, _ = _host_call(w, x)
     assert_parity(w, oh.double().numpy(), lh.double().numpy(), ro, rl, f"{prob} attn_fwd_host")
+
+
+# ------------------------------------------------------------------ key-split last round
+SPLIT_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, D, dtype, causal, qk_std: few enough equal-length items that
+    # the plan cuts the last (here: only) round into key ranges
+    (1, 4, 2, 3000, 3000, 128, "bf16", False, 1.0),   # 48 items, ragged keys
+    (1, 8, 2, 700, 9000, 128, "bf16", True, 1.0),     # a chunk over a longer cache
+    (2, 2, 1, 1000, 1000, 64, "f16", False, 2.0),
+    (1, 4, 4, 300, 5000, 128, "f16", True, 4.0),      # near-one-hot rows, causal offset 4700
+    (1, 2, 1, 129, 2000, 128, "bf16", True, 1.0),     # ragged query tile
+]
+
+
+def _split_workload(shape):
+    B, Hq, Hkv, Nq, Nk, D, dtype, causal, std = shape
+    return workloads.Workload("split", B, Hq, Hkv, Nq, D, dtype, causal, q_std=std, k_std=std,
+                              seed=zlib.crc32(repr(shape).encode()) & 0xFFFF, Nk=Nk)
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_split_shapes(shape):
+    """attn_fwd_kv_split cuts these items into key ranges and merges the pieces: every row
+    against the oracle, and within tolerance of the uncut call."""
+    import torch
+
+    w = _split_workload(shape)
+    st, nbytes = binding.attn_fwd_kv_split_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D, w.causal)
+    assert st == binding.ATTN_OK and nbytes > 0, "the plan should cut this problem"
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o, lse = binding.attention_split(q, k, v, causal=w.causal, scale=w.scale)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    err = assert_parity(w, _np(o), _np(lse), ro, rl, str(shape))
+    o2, l2 = binding.attention(q, k, v, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert float((o.float() - o2.float()).abs().max()) <= (2e-3 if w.dtype == "f16" else 1.6e-2)
+    assert float(((lse - l2).abs() / l2.abs().clamp_min(1.0)).max()) <= 1e-4
+    print(f"{shape}: max|dO|={err[0]:.3e} max rel dLSE={err[1]:.3e}")
+
+
+def test_split_workspace_sizes():
+    """Causal problems with Nq == Nk are not cut (their items already differ in length);
+    a problem that fills many rounds exactly is not cut either."""
+    st, n = binding.attn_fwd_kv_split_workspace(1, 32, 8, 32768, 32768, 128, True)
+    assert st == binding.ATTN_OK and n == 0
+    st, n = binding.attn_fwd_kv_split_workspace(4, 32, 8, 4096, 4096, 128, False)
+    assert st == binding.ATTN_OK and n > 0  # 2048 items: the 14th round holds 72
+
+
+def test_split_repeated_calls_and_graph_replays():
+    """One workspace, calls in a row with new inputs, then a captured call replayed twice on
+    new inputs (the arrival counters carry the launch's sequence number, and the last
+    arrival leaves them at zero for the next replay)."""
+    import torch
+
+    w = _split_workload(SPLIT_SHAPES[0])
+    st, nbytes = binding.attn_fwd_kv_split_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D, w.causal)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    xs = [workloads.make_inputs(w, seed=w.seed + t) for t in range(4)]
+    q, k, v = (to_device(xs[0][n], w.dtype) for n in "qkv")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+
+    def call():
+        binding.attention_split(q, k, v, causal=w.causal, scale=w.scale, workspace=ws, out=o,
+                                lse_out=lse)
+
+    def check(x, what):
+        torch.cuda.synchronize()
+        assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+        ro, rl = oracle_full(w, x)
+        assert_parity(w, _np(o), _np(lse), ro, rl, what)
+
+    for t in range(2):
+        for name, tt in zip("qkv", (q, k, v)):
+            tt.copy_(to_device(xs[t][name], w.dtype))
+        call()
+        check(xs[t], f"call {t}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for t in (2, 3):
+        for name, tt in zip("qkv", (q, k, v)):
+            tt.copy_(to_device(xs[t][name], w.dtype))
+        graph.replay()
+        check(xs[t], f"replay {t}")
+
+
+def test_split_timeout_is_reported_and_context_survives():
+    """The split path under a wait nothing satisfies: ATTN_ERR_TIMEOUT, and the next call
+    (new launch sequence number, same workspace) is correct."""
+    import torch
+
+    lib = binding.load()
+    w = _split_workload(SPLIT_SHAPES[2])
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    st, nbytes = binding.attn_fwd_kv_split_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D, w.causal)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    try:
+        lib.attn_test_set_wait_timeout_ns(300_000_000)
+        lib.attn_test_inject_stall(1)
+        binding.attention_split(q, k, v, causal=w.causal, scale=w.scale, workspace=ws)
+        st = binding.attn_last_device_error(torch.cuda.current_stream())
+    finally:
+        lib.attn_test_inject_stall(0)
+        lib.attn_test_set_wait_timeout_ns(0)
+    assert st == binding.ATTN_ERR_TIMEOUT
+    o, lse = binding.attention_split(q, k, v, causal=w.causal, scale=w.scale, workspace=ws)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    ro, rl = oracle_full(w, x)
+    assert_parity(w, _np(o), _np(lse), ro, rl, "split after timeout")
+
+
+@pytest.mark.parametrize("name", ["noncausal_gqa_bf16_n4096", "chunked_prefill_causal_gqa_bf16_q4096_k32768"])
+def test_split_full_size_every_row(name):
+    """The two equal-length benchmark workloads through attn_fwd_kv_split (their last
+    round is cut in two): every row against the oracle."""
+    import torch
+
+    w = workloads.WORKLOADS[name]
+    st, nbytes = binding.attn_fwd_kv_split_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D, w.causal)
+    assert st == binding.ATTN_OK and nbytes > 0
+    x = workloads.make_inputs(w)
+    q, k, v = (to_device(x[n], w.dtype) for n in "qkv")
+    o, lse = binding.attention_split(q, k, v, causal=w.causal, scale=w.scale)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    og, lg = _np(o), _np(lse)
+    del o, lse
+    ro, rl = oracle_full(w, x)
+    err = assert_parity(w, og, lg, ro, rl, name + " split")
+    record({"workload": name + " (attn_fwd_kv_split)", "rows": w.B * w.Hq * w.N, "max_abs_dO": err[0],
+            "max_rel_dLSE": err[1], "max_dO_ulps": ulp_error(og, ro, w.dtype)})
