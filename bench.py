@@ -64,6 +64,9 @@ def parse_args():
                          "that grows with the ranks; strong: the ranks split one workload")
     ap.add_argument("--item-order", type=int, choices=[0, 1], default=None,
                     help="work-item order of the persistent kernel (library default if unset)")
+    ap.add_argument("--launch-only", type=int, default=0, metavar="N",
+                    help="only N launches of the workload, each after a 256 MB L2 flush, and no "
+                         "output (a target for ncu: -s N-1 -c 1 captures the last launch)")
     return ap.parse_args()
 
 
@@ -593,8 +596,52 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_launch_only(args):
+    """N launches of the workload's C entry point with L2 flushed before each."""
+    import torch
+
+    from gqa_attention_forward_gb300 import binding
+
+    w = workloads.WORKLOADS[args.workload]
+    device = torch.device("cuda", torch.cuda.current_device())
+    x = workloads.make_inputs(w)
+    q, k, v = (to_dev(x[n], w.dtype, device) for n in "qkv")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=device)
+    s = torch.cuda.current_stream(device)
+    dcode = binding.ATTN_BF16 if w.dtype == "bf16" else binding.ATTN_F16
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    ws, nbytes = None, 0
+    if w.entry == "attn_fwd_kv_split":
+        st, nbytes = binding.attn_fwd_kv_split_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D, w.causal)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    elif w.entry == "attn_fwd_decode":
+        st, nbytes = binding.attn_fwd_decode_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    for _ in range(args.launch_only):
+        flush.zero_()
+        if w.entry == "attn_fwd_kv_split":
+            st = binding.attn_fwd_kv_split(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
+                                           w.scale, w.causal, dcode, ws, nbytes, s)
+        elif w.entry == "attn_fwd_decode":
+            st = binding.attn_fwd_decode(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
+                                         w.scale, w.causal, dcode, ws, nbytes, s)
+        else:
+            st = binding.attn_fwd_kv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D,
+                                     w.scale, w.causal, dcode, s)
+        if st != binding.ATTN_OK:
+            raise binding.AttnError(st, w.entry)
+    torch.cuda.synchronize()
+    st = binding.attn_last_device_error(s)
+    if st != binding.ATTN_OK:
+        raise binding.AttnError(st, "launch-only")
+
+
 def main():
     args = parse_args()
+    if args.launch_only > 0:
+        run_launch_only(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
