@@ -536,8 +536,9 @@ def _random_problems(count=24, seed=2024):
 
 @pytest.mark.parametrize("prob", _random_problems(), ids=lambda p: "x".join(map(str, p)))
 def test_random_problems_all_entry_points(prob):
-    """Seeded random problems through attn_fwd_kv, attn_fwd_decode and attn_fwd_host,
-    each against the oracle."""
+    """Seeded random problems through attn_fwd_kv, attn_fwd_decode, attn_fwd_host and
+    attn_fwd_kv_split (which cuts the last round into key ranges when it can), each
+    against the oracle."""
     import torch
 
     t, B, Hq, Hkv, Nq, Nk, D, dtype, causal, std = prob
@@ -553,6 +554,9 @@ def test_random_problems_all_entry_points(prob):
     assert_parity(w, _np(o2), _np(l2), ro, rl, f"{prob} attn_fwd_decode")
     oh, lh, _, _ = _host_call(w, x)
     assert_parity(w, oh.double().numpy(), lh.double().numpy(), ro, rl, f"{prob} attn_fwd_host")
+    o3, l3 = binding.attention_split(q, k, v, causal=causal, scale=w.scale)
+    assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+    assert_parity(w, _np(o3), _np(l3), ro, rl, f"{prob} attn_fwd_kv_split")
 
 
 # ------------------------------------------------------------------ key-split last round
