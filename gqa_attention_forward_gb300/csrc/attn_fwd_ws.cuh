@@ -49,7 +49,7 @@ constexpr uint32_t kWsTmemCols = 512;
 // A warp's 32 rows of probabilities are split into two input-type terms
 // (P_hi + P_lo) when some row's running sum, in units of its largest weight,
 // is below this.
-constexpr float kSplitL = 16.f;
+constexpr float kSplitL = 4.f;
 // The probabilities are referenced to a stale row max until the true max
 // exceeds it by more than this many powers of two (P <= 2^8 meanwhile).
 constexpr float kRescaleLog2 = 8.f;
