@@ -446,6 +446,48 @@ def test_decode_timeout_is_reported_and_context_survives(forced_splits):
     assert_parity(w, _np(o), _np(lse), ro, rl, "decode after timeout")
 
 
+def test_decode_repeated_calls_and_graph_replays(forced_splits):
+    """The split kernel and the merge kernel of attn_fwd_decode (programmatic dependent
+    launches): one workspace, calls in a row with new inputs, then a captured call
+    replayed twice on new inputs."""
+    import torch
+
+    forced_splits(6)
+    w = workloads.Workload("drep", 2, 16, 4, 5, 128, "bf16", True, seed=34, Nk=3000)
+    st, nbytes = binding.attn_fwd_decode_workspace(w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D)
+    assert st == binding.ATTN_OK and nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    xs = [workloads.make_inputs(w, seed=w.seed + t) for t in range(4)]
+    q, k, v = (to_device(xs[0][n], w.dtype) for n in "qkv")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+
+    def call():  # on torch's current stream (the capture stream inside the graph block)
+        assert binding.attn_fwd_decode(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.n_keys, w.D, w.scale,
+                                       1, q.dtype, ws, ws.numel(),
+                                       torch.cuda.current_stream()) == binding.ATTN_OK
+
+    def check(x, what):
+        torch.cuda.synchronize()
+        assert binding.attn_last_device_error(torch.cuda.current_stream()) == binding.ATTN_OK
+        ro, rl = oracle_full(w, x)
+        assert_parity(w, _np(o), _np(lse), ro, rl, what)
+
+    for t in range(2):
+        for name, tt in zip("qkv", (q, k, v)):
+            tt.copy_(to_device(xs[t][name], w.dtype))
+        call()
+        check(xs[t], f"call {t}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for t in (2, 3):
+        for name, tt in zip("qkv", (q, k, v)):
+            tt.copy_(to_device(xs[t][name], w.dtype))
+        graph.replay()
+        check(xs[t], f"replay {t}")
+
+
 # ------------------------------------------------------------------ host buffers
 def _host_call(w, x, pinned=True):
     """attn_fwd_host on host copies of the inputs; returns (o, lse) as host tensors and
