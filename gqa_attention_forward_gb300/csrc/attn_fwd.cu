@@ -491,7 +491,15 @@ attn_status_t launch_decode(int dev, int kid, const gqa::Params &prm, cudaStream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+    // Q as [B*Hkv, G*Nq, D]: the packed rows of one kv head are one block
+    CUtensorMap tq, tk, tv;
+    const long long BHkv = prm.BHq / prm.group;
+    if (!encode_rows_map(&tq, prm.q, BF16, D, prm.rows_per_kv, BHkv) ||
+        !encode_rows_map(&tk, prm.k, BF16, D, prm.Nk, BHkv) || !encode_rows_map(&tv, prm.v, BF16, D, prm.Nk, BHkv)) {
+        std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
+        return ATTN_ERR_LAUNCH;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, prm);
     if (e == cudaSuccess && prm.n_splits > 1) {
         cfg.gridDim = dim3(static_cast<unsigned>((prm.total_rows + 3) / 4));
         cfg.blockDim = dim3(128);

@@ -19,7 +19,7 @@
 // applied across CTAs instead of across the tiles of one CTA.  With one split
 // the first kernel writes O and LSE itself and no workspace is used.
 //
-// Roles (256 threads): warps 2-3 load (cp.async, 4-stage ring), warp 1 issues
+// Roles (256 threads): warp 2 lane 0 loads (TMA, 4-stage ring), warp 1 issues
 // the MMAs (S = Q K^T and O += P V into TMEM), warps 4-7 run the softmax of
 // one row each and stage P through shared memory.  S has two TMEM buffers and
 // P two shared-memory buffers, so the tensor core computes S(j+1) while the
@@ -28,6 +28,8 @@
 // largest weight of a row is exactly 1 and near one-hot rows keep their
 // ratios through P's rounding.
 #pragma once
+#include <cuda.h>  // CUtensorMap
+
 #include "kernel_common.cuh"
 
 namespace gqa {
@@ -64,9 +66,13 @@ __device__ __forceinline__ PosRange tile_positions(int m0, int rows, int Nq) {
     return a <= b ? PosRange{a, b} : PosRange{0, Nq - 1};
 }
 
+// tmQ: 3-D tensor map (D, rows_per_kv, B*Hkv) of Q seen as [B*Hkv, G*Nq, D] (the
+// packed rows of each kv head); tmK, tmV: (D, Nk, B*Hkv).  Box 64 x 128 x 1 with the
+// 128-byte swizzle; rows past the end of a kv head's block read as zeros.
 template <int D, bool kBF16, bool kCausal>
 __global__ void __launch_bounds__(kDecThreads, 1)
-    attn_fwd_decode_kernel(const Params p) {
+    attn_fwd_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const Params p) {
     using L = DecLayout<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = static_cast<int>(blockIdx.x % p.n_splits);
@@ -125,9 +131,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_abort_seq) == p.seq) ? 1 : 0;
-        mbar_init(q_full, kLoaderThreads);
+        mbar_init(q_full, 1);
         for (int s = 0; s < kDecStages; ++s) {
-            mbar_init(kv_full(s), kLoaderThreads);
+            mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
         }
         mbar_init(s_full(0), 1);
@@ -150,36 +156,42 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint32_t tmem = *tmem_slot;
     grid_dependency_wait();  // the set-up above overlapped the previous kernel's tail
 
-    if (warp >= 2 && warp < 4) {
-        // ---------------------------------------------------- loaders (warps 2, 3)
-        const int ltid = threadIdx.x - 64;
-        const size_t kv_head_bytes = static_cast<size_t>(p.Nk) * D * 2;
-        const uint8_t *kh = p.k + static_cast<size_t>(bkv) * kv_head_bytes;
-        const uint8_t *vh = p.v + static_cast<size_t>(bkv) * kv_head_bytes;
-        // each thread's copies arrive on a tile's full barrier when they land
-        // (kLoaderThreads arrivals complete it), so the whole ring can be in flight
-        if (!p.inject_stall) {
-            load_tile<D>(sQ, p.q + base_row * (D * 2), m0, p.rows_per_kv, ltid);
-            cp_async_arrive(q_full);
+    if (warp == 2) {
+        if (lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            // One tile = D/64 boxes of 128 rows x 64 columns (x = 64a: a multiple of
+            // 16 bytes); its full barrier expects all of its bytes.
+            auto load_tile_tma = [&](uint32_t dst, const CUtensorMap *tm, int row, uint32_t bar) {
+                mbar_arrive_expect_tx(bar, L::kTileBytes);
+#pragma unroll
+                for (int a = 0; a < D / 64; ++a) tma_load_3d(dst + a * kAtomBytes, tm, 64 * a, row, bkv, bar);
+            };
+            const bool q_loaded = !p.inject_stall;
+            if (q_loaded) load_tile_tma(sQ, &tmQ, m0, q_full);
+            int stage = 0, loads = 0;
+            uint32_t phase = 0;
+            auto load = [&](const CUtensorMap *tm, int j) -> bool {
+                if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) return false;
+                load_tile_tma(sKV + stage * L::kTileBytes, tm, (kt0 + j) * kBN, kv_full(stage));
+                ++loads;
+                if (++stage == kDecStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                return true;
+            };
+            // the MMA warp's order: K_0, K_1, then V_j, K_{j+2} for each j
+            bool ok = load(&tmK, 0) && (n_kv < 2 || load(&tmK, 1));
+            for (int j = 0; j < n_kv && ok; ++j) ok = load(&tmV, j) && (j + 2 >= n_kv || load(&tmK, j + 2));
+            // Every copy has landed before the CTA exits (also after a timeout).  The
+            // ring is filled in order, so stage st last received a copy in the current
+            // lap (phase) if st < stage, else in the lap before.
+#pragma unroll
+            for (int st = 0; st < kDecStages; ++st)
+                if (loads > st) drain_bar(kv_full(st), st < stage ? phase : phase ^ 1u, p);
+            if (q_loaded) drain_bar(q_full, 0, p);
         }
-        int stage = 0;
-        uint32_t phase = 0;
-        auto load = [&](const uint8_t *head, int j) -> bool {
-            if (!wait_bar(kv_empty(stage), phase ^ 1u, p, abort_flag)) return false;
-            load_tile<D>(sKV + stage * L::kTileBytes, head, (kt0 + j) * kBN, p.Nk, ltid);
-            cp_async_arrive(kv_full(stage));
-            if (++stage == kDecStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            return true;
-        };
-        // the MMA warp's order: K_0, K_1, then V_j, K_{j+2} for each j
-        bool ok = load(kh, 0) && (n_kv < 2 || load(kh, 1));
-        for (int j = 0; j < n_kv && ok; ++j) ok = load(vh, j) && (j + 2 >= n_kv || load(kh, j + 2));
-        // every copy has landed before the CTA exits
-        cp_async_commit();
-        cp_async_wait<0>();
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------------------------------------------- MMA issuer
@@ -187,7 +199,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, kBM, D, true);
             const uint32_t tO = tmem + kDecTmemO;
             bool ok = wait_bar(q_full, 0, p, abort_flag);
-            fence_proxy_async_smem();  // cp.async data -> tensor core reads
             tc_fence_after();
             int stage = 0;
             uint32_t phase = 0;
@@ -202,7 +213,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             // S_b = Q K^T into TMEM buffer b (A = Q, B = K: both K-major, 128-byte swizzle)
             auto qk = [&](int b) -> bool {
                 if (!wait_bar(kv_full(stage), phase, p, abort_flag)) return false;
-                fence_proxy_async_smem();
                 tc_fence_after();
                 const int ks = stage;
                 const uint32_t sK = next_stage();
@@ -224,7 +234,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 if (!(ok = wait_bar(p_full, j & 1, p, abort_flag))) break;
                 tc_fence_after();
                 if (!(ok = wait_bar(kv_full(stage), phase, p, abort_flag))) break;
-                fence_proxy_async_smem();
                 tc_fence_after();
                 const int vs = stage;
                 const uint32_t sV = next_stage();
