@@ -108,7 +108,7 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, const P
     }
 }
 
-constexpr int kLoaderThreads = 64;  // warps 2 and 3 of either kernel
+constexpr int kLoaderThreads = 64;  // warps 2 and 3 of the per-tile cross-check kernel
 constexpr int kAtomBytes = 128 * 128;  // 128 rows x 128 B: one 128-byte swizzle atom column
 
 // Copies rows [row0, row0 + 128) of one head ([N, D], 2-byte elements, D
