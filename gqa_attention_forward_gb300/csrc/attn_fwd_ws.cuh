@@ -8,8 +8,10 @@
 // Roles (384 threads):
 //   warp 2        TMA producer (one lane): K_0, (Q0, Q1), V_0, K_1, V_1, ... as
 //                 128-row boxes of 64 columns with the 128-byte swizzle, into a
-//                 ring of kStagesWs tiles (full / empty mbarriers; each full
-//                 barrier expects the tile's bytes as a transaction count).
+//                 ring of kStagesWs tiles (full / empty mbarriers).  A unit's
+//                 first K tile completes its own full barrier; V_j and K_{j+1}
+//                 complete V_j's together (its transaction count is both tiles'
+//                 bytes), so the MMA warp waits once per key tile.
 //   warp 1        allocates and frees the 512 TMEM columns.
 //   warp 0        MMA issuer (one lane):  S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per
 //                 key tile j:  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,
@@ -252,11 +254,43 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
                 for (int a = 0; a < L::kAtoms; ++a) tma_load_3d(dst + a * kAtomBytes, tm, 64 * a, row, head, bar);
             };
-            auto load_kv = [&](const CUtensorMap *tm, int row, int head) -> bool {
+            // Full barriers: the first K tile of a unit completes its own stage's
+            // barrier; V_j and K_{j+1} both complete V_j's, so the MMA warp waits once
+            // per key tile.  Stages are then not armed once per lap, so each keeps its
+            // own phase bit (fph), as the MMA warp does.
+            uint32_t fph = 0, armed = 0;
+            auto issue = [&](uint32_t dst, const CUtensorMap *tm, int row, int head, uint32_t bar) {
+#pragma unroll
+                for (int a = 0; a < L::kAtoms; ++a) tma_load_3d(dst + a * kAtomBytes, tm, 64 * a, row, head, bar);
+            };
+            auto load_k_first = [&](int row, int head) -> bool {
                 if (!wait_bar(kv_empty(ring.s), ring.ph ^ 1u, p, abort_flag)) return false;
-                load_tile_tma(sKV + ring.s * L::kTileBytes, tm, row, head, kv_full(ring.s));
+                mbar_arrive_expect_tx(kv_full(ring.s), L::kTileBytes);
+                armed |= 1u << ring.s;
+                fph ^= 1u << ring.s;
+                issue(sKV + ring.s * L::kTileBytes, &tmK, row, head, kv_full(ring.s));
                 ++kv_loads;
                 ring.next();
+                return true;
+            };
+            // V_j, and K_{j+1} when `pair`, on V_j's barrier
+            auto load_vk = [&](int j, bool pair, int head) -> bool {
+                const int vs = ring.s;
+                if (!wait_bar(kv_empty(vs), ring.ph ^ 1u, p, abort_flag)) return false;
+                Ring nr = ring;
+                nr.next();
+                if (pair && !wait_bar(kv_empty(nr.s), nr.ph ^ 1u, p, abort_flag)) return false;
+                mbar_arrive_expect_tx(kv_full(vs), L::kTileBytes * (pair ? 2u : 1u));
+                armed |= 1u << vs;
+                fph ^= 1u << vs;
+                issue(sKV + vs * L::kTileBytes, &tmV, j * kBN, head, kv_full(vs));
+                ring.next();
+                ++kv_loads;
+                if (pair) {
+                    issue(sKV + ring.s * L::kTileBytes, &tmK, (j + 1) * kBN, head, kv_full(vs));
+                    ring.next();
+                    ++kv_loads;
+                }
                 return true;
             };
             int q_loads = 0;
@@ -268,7 +302,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const KeyRange kr = ws_range<kCausal>(p, qb, part);
                 // The first K tile may land while the previous unit still runs; the Q
                 // buffers are free once every S MMA of the previous unit is done.
-                if (!(ok = load_kv(&tmK, kr.k0 * kBN, kvh))) break;
+                if (!(ok = load_k_first(kr.k0 * kBN, kvh))) break;
                 if (!(ok = wait_bar(q_empty, (items & 1) ^ 1u, p, abort_flag))) break;
                 if (!p.inject_stall) {
                     load_tile_tma(sQ, &tmQ, q0, bh, q_full(0));
@@ -286,17 +320,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         tma_prefetch_l2_3d(&tmQ, 64 * a, nqb * 256 + 128, nbh);
                     }
                 }
-                for (int j = kr.k0; j < kr.e1 && ok; ++j) {
-                    ok = load_kv(&tmV, j * kBN, kvh);
-                    if (ok && j + 1 < kr.e1) ok = load_kv(&tmK, (j + 1) * kBN, kvh);
-                }
+                for (int j = kr.k0; j < kr.e1 && ok; ++j) ok = load_vk(j, j + 1 < kr.e1, kvh);
             }
-            // Every copy has landed before the CTA exits (also after a timeout).  The
-            // ring is filled in order, so stage st last received a copy in the current
-            // lap (phase ring.ph) if st < ring.s, else in the lap before.
+            // Every copy has landed before the CTA exits (also after a timeout): wait for
+            // the last armed phase of every stage's full barrier.
 #pragma unroll
             for (int st = 0; st < kStagesWs; ++st)
-                if (kv_loads > st) drain_bar(kv_full(st), st < ring.s ? ring.ph : ring.ph ^ 1u, p);
+                if ((armed >> st) & 1u) drain_bar(kv_full(st), ((fph >> st) & 1u) ^ 1u, p);
             if (q_loads > 0) {
                 drain_bar(q_full(0), (q_loads - 1) & 1, p);
                 drain_bar(q_full(1), (q_loads - 1) & 1, p);
@@ -306,6 +336,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             constexpr uint32_t idesc_qk = idesc_f16_f32acc(kBF16, 128, kBN, false);
             constexpr uint32_t idesc_pv = idesc_f16_f32acc(kBF16, 128, D, true);
             Ring ring;
+            uint32_t fph = 0;  // per-stage phase of the full barriers, as the producer arms them
+            auto wait_full = [&](int st) -> bool {
+                const bool r = wait_bar(kv_full(st), (fph >> st) & 1u, p, abort_flag);
+                fph ^= 1u << st;
+                return r;
+            };
             uint32_t pcount[2] = {0, 0};
             int items = 0;
             bool ok = true;
@@ -358,7 +394,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const int k0 = kr.k0, n0 = kr.e0, n1 = kr.e1;  // tiles [k0, n0) and [k0, n1)
                 const uint32_t ip = items & 1;
                 if (!(ok = wait_bar(q_full(0), ip, p, abort_flag))) break;
-                if (!(ok = wait_bar(kv_full(ring.s), ring.ph, p, abort_flag))) break;
+                if (!(ok = wait_full(ring.s))) break;
                 tc_fence_after();
                 qk(0, ring.s);
                 mma_commit(s_full(0));
@@ -370,7 +406,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 ring.next();
                 for (int j = k0; j < n1; ++j) {
                     const int vs = ring.s;
-                    if (!(ok = wait_bar(kv_full(vs), ring.ph, p, abort_flag))) break;
+                    if (!(ok = wait_full(vs))) break;  // V_j, and K_{j+1} if any
+                    tc_fence_after();
                     ring.next();
                     if (j < n0) {
                         if (!(ok = wait_bar(p_full(0), pcount[0] & 1u, p, abort_flag))) break;
@@ -382,8 +419,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const bool more = j + 1 < n1;
                     const int ks = ring.s;
                     if (more) {
-                        if (!(ok = wait_bar(kv_full(ks), ring.ph, p, abort_flag))) break;
-                        tc_fence_after();
                         if (j + 1 < n0) {
                             qk(0, ks);
                             mma_commit(s_full(0));
