@@ -246,7 +246,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             Ring ring;
             int items = 0;
             bool ok = true;
-            int kv_loads = 0;  // K/V tiles issued so far (ring position = kv_loads mod stages)
             // One tile = D/64 boxes of 128 rows x 64 columns (128 bytes, x = 64a:
             // a multiple of 16 bytes); the full barrier expects all of its bytes.
             auto load_tile_tma = [&](uint32_t dst, const CUtensorMap *tm, int row, int head, uint32_t bar) {
@@ -269,7 +268,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 armed |= 1u << ring.s;
                 fph ^= 1u << ring.s;
                 issue(sKV + ring.s * L::kTileBytes, &tmK, row, head, kv_full(ring.s));
-                ++kv_loads;
                 ring.next();
                 return true;
             };
@@ -285,11 +283,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 fph ^= 1u << vs;
                 issue(sKV + vs * L::kTileBytes, &tmV, j * kBN, head, kv_full(vs));
                 ring.next();
-                ++kv_loads;
                 if (pair) {
                     issue(sKV + ring.s * L::kTileBytes, &tmK, (j + 1) * kBN, head, kv_full(vs));
                     ring.next();
-                    ++kv_loads;
                 }
                 return true;
             };
